@@ -1,0 +1,8 @@
+"""Float64 CPU oracle of scaled dot-product attention.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
+benchmark's CPU-baseline leg, never by the library.
+"""
+from .sdpa_oracle import (  # noqa: F401
+    causal_bias, default_scale, ref_backward, ref_forward, ref_forward_rows, ref_group,
+)

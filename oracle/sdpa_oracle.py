@@ -1,0 +1,278 @@
+"""Float64 CPU oracle for scaled dot-product attention (forward, backward, decode).
+
+TEST INFRASTRUCTURE ONLY.  This module is the plain, slow, obviously correct
+definition that the CUDA library is checked against.  Only the test suite,
+the smoke check and the benchmark's CPU-baseline leg may import it; the
+library itself never does, and it shares no code with the CUDA path.
+
+Everything is NumPy float64, one (batch, query head) problem at a time, in the
+order and notation of the course chapter "Scaled dot-product attention
+(forward and backward)": scores S = alpha*Q*K^T, masked softmax P, output
+O = P*V, and the hand-derived backward of its section 2.3.
+
+Sources for each step (page title, section):
+  * definition O = softmax(alpha*Q*K^T + mask)*V and the default scale
+    1/sqrt(d): "Scaled dot-product attention (forward and backward)",
+    Key Takeaways and section 2.1;
+  * additive mask, -inf where blocked, applied before the softmax, and an
+    all-blocked row giving zeros: same page, section 2.2, and
+    "ScaledDotProductAttentionBackward" (Notes: additive mask, engine-side
+    causal j <= i);
+  * causal = lower triangle tril(diagonal=0), top-left aligned:
+    "Understanding PyTorch Scaled Dot-Product Attention", section 3;
+  * grouped-query heads by repeat_interleave (query head h reads KV head
+    floor(h / (Hq/Hkv))): same page, section 4;
+  * backward dV = P^T dO, dP = dO V^T, dS = P o (dP - D), D_i = sum_j P_ij dP_ij
+    = dO_i . O_i, dQ = alpha dS K, dK = alpha dS^T Q: "Scaled dot-product
+    attention (forward and backward)", section 2.3;
+  * log-sum-exp statistics max + ln(sum exp(s - max)), natural log, fp32
+    shape (B, Hq, L): "Attention" (cuDNN), Scaled Dot Product Attention,
+    Returns ("stats").
+
+Readings where the pages are silent (every one also listed in the design notes):
+  * a fully blocked row has LSE = -inf, O = 0, dQ = 0 and contributes nothing
+    to dK/dV;
+  * the scale multiplies Q*K^T only, never the mask;
+  * only -inf blocks; a finite large negative number is just a number.
+
+Every function here is pinned by tests against the page's hand-worked
+example, central differences, invariants and a library cross-check.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "default_scale", "ref_forward", "ref_backward", "ref_forward_rows",
+    "ref_group", "causal_bias",
+]
+
+NEG_INF = -np.inf
+
+
+def default_scale(E: int) -> float:
+    """Default alpha = 1/sqrt(d) (course chapter, section 2.1 "Why scale?")."""
+    return 1.0 / math.sqrt(E)
+
+
+def _scores(q: np.ndarray, k: np.ndarray, alpha: float) -> np.ndarray:
+    """S = alpha * Q K^T, [L, S] (course chapter, symbol table of section 2)."""
+    return alpha * (q @ k.T)
+
+
+def causal_bias(L: int, S: int) -> np.ndarray:
+    """Engine-side causal mask: 0 where j <= i, -inf where j > i (top-left tril)."""
+    i = np.arange(L)[:, None]
+    j = np.arange(S)[None, :]
+    return np.where(j <= i, 0.0, NEG_INF)
+
+
+def _masked_softmax(s: np.ndarray, bias: np.ndarray):
+    """Row softmax of s + bias over the keys, stable, all -inf rows -> zeros.
+
+    Returns (P, lse) with lse_i = m_i + ln(sum_j exp(t_ij - m_i)) and -inf
+    for a row with every key blocked (course chapter, section 2.2; cuDNN
+    "Attention" page, stats).
+    """
+    t = s + bias
+    m = t.max(axis=1)
+    open_row = np.isfinite(m)
+    m_safe = np.where(open_row, m, 0.0)
+    e = np.exp(t - m_safe[:, None])            # exp(-inf) = 0 exactly
+    z = e.sum(axis=1)
+    P = np.zeros_like(t)
+    P[open_row] = e[open_row] / z[open_row, None]
+    lse = np.full(t.shape[0], NEG_INF)
+    lse[open_row] = m[open_row] + np.log(z[open_row])
+    return P, lse
+
+
+def _row_D(P: np.ndarray, dP: np.ndarray) -> np.ndarray:
+    """D_i = sum_j P_ij dP_ij (course chapter, section 2.3)."""
+    return (P * dP).sum(axis=1)
+
+
+def _softmax_vjp(P: np.ndarray, dP: np.ndarray, D: np.ndarray) -> np.ndarray:
+    """dS = P o (dP - D) (course chapter, section 2.3)."""
+    return P * (dP - D[:, None])
+
+
+def _dq(dS: np.ndarray, k: np.ndarray, alpha: float) -> np.ndarray:
+    """dQ = alpha dS K (course chapter, section 2.3)."""
+    return alpha * (dS @ k)
+
+
+def _dk(dS: np.ndarray, q: np.ndarray, alpha: float) -> np.ndarray:
+    """dK = alpha dS^T Q (course chapter, section 2.3; note the transpose)."""
+    return alpha * (dS.T @ q)
+
+
+def _as64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):                   # a torch tensor (bf16 is upcast exactly)
+        x = x.detach().to("cpu")
+        import torch  # local: only to read the tensor's values
+        x = x.to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _check_shapes(q, k, v, mask, enable_gqa):
+    B, Hq, L, E = q.shape
+    Bk, Hkv, S, Ek = k.shape
+    if k.ndim != 4 or q.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be [B, H, T, D]")
+    if Bk != B or v.shape[0] != B:
+        raise ValueError("batch sizes differ")
+    if Ek != E:
+        raise ValueError("q and k widths differ")
+    if v.shape[1] != Hkv or v.shape[2] != S:
+        raise ValueError("k and v disagree on heads or length")
+    if Hq != Hkv and not enable_gqa:
+        raise ValueError("Hq != Hkv needs enable_gqa")
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if mask is not None:
+        if mask.ndim != 4 or mask.shape[2:] != (L, S) or mask.shape[0] not in (1, B) \
+                or mask.shape[1] not in (1, Hq):
+            raise ValueError("mask must be [B|1, Hq|1, L, S]")
+    return B, Hq, Hkv, L, S, E, v.shape[3]
+
+
+def _head_bias(mask, b, h, L, S, is_causal):
+    bias = np.zeros((L, S))
+    if mask is not None:
+        bias = bias + mask[min(b, mask.shape[0] - 1), min(h, mask.shape[1] - 1)]
+    if is_causal:
+        bias = bias + causal_bias(L, S)
+    return bias
+
+
+def _alpha(scale, E):
+    if scale is None:
+        return default_scale(E)
+    if not (scale >= 0.0) or math.isinf(scale):
+        raise ValueError("scale must be finite and >= 0")
+    return float(scale)
+
+
+def _head_forward(q, k, v, bias, alpha):
+    P, lse = _masked_softmax(_scores(q, k, alpha), bias)
+    return P @ v, lse, P
+
+
+def ref_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=False,
+                return_P=False):
+    """O [B,Hq,L,Ev] and LSE [B,Hq,L] of softmax(alpha*Q*K^T + mask + causal)*V.
+
+    Query head h reads KV head h // (Hq // Hkv) (repeat_interleave).
+    """
+    q, k, v, mask = _as64(q), _as64(k), _as64(v), _as64(mask)
+    B, Hq, Hkv, L, S, E, Ev = _check_shapes(q, k, v, mask, enable_gqa)
+    G = Hq // Hkv
+    alpha = _alpha(scale, E)
+    O = np.zeros((B, Hq, L, Ev))
+    LSE = np.zeros((B, Hq, L))
+    Ps = np.zeros((B, Hq, L, S)) if return_P else None
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // G
+            o, lse, P = _head_forward(q[b, h], k[b, kv], v[b, kv],
+                                      _head_bias(mask, b, h, L, S, is_causal), alpha)
+            O[b, h], LSE[b, h] = o, lse
+            if return_P:
+                Ps[b, h] = P
+    return (O, LSE, Ps) if return_P else (O, LSE)
+
+
+def _head_backward(q, k, v, P, o, dO, alpha):
+    dV = P.T @ dO
+    dP = dO @ v.T
+    D = _row_D(P, dP)
+    # the identity D_i = dO_i . O_i of section 2.3 must hold for the oracle's own P
+    np.testing.assert_allclose(D, (dO * o).sum(axis=1), rtol=1e-9, atol=1e-9)
+    dS = _softmax_vjp(P, dP, D)
+    return _dq(dS, k, alpha), _dk(dS, q, alpha), dV, D
+
+
+def ref_backward(q, k, v, dO, mask=None, scale=None, is_causal=False, enable_gqa=False,
+                 return_D=False):
+    """dQ [B,Hq,L,E], dK [B,Hkv,S,E], dV [B,Hkv,S,Ev] of L = sum(O * dO).
+
+    dK and dV of a KV head are summed over the Hq/Hkv query heads that read it
+    (chain rule through repeat_interleave).  P is recomputed from the
+    definition, never taken from another implementation.
+    """
+    q, k, v, dO, mask = _as64(q), _as64(k), _as64(v), _as64(dO), _as64(mask)
+    B, Hq, Hkv, L, S, E, Ev = _check_shapes(q, k, v, mask, enable_gqa)
+    G = Hq // Hkv
+    alpha = _alpha(scale, E)
+    dQ = np.zeros((B, Hq, L, E))
+    dK = np.zeros((B, Hkv, S, E))
+    dV = np.zeros((B, Hkv, S, Ev))
+    Dall = np.zeros((B, Hq, L))
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // G
+            bias = _head_bias(mask, b, h, L, S, is_causal)
+            o, _, P = _head_forward(q[b, h], k[b, kv], v[b, kv], bias, alpha)
+            dq, dk, dv, D = _head_backward(q[b, h], k[b, kv], v[b, kv], P, o, dO[b, h], alpha)
+            dQ[b, h] = dq
+            dK[b, kv] += dk
+            dV[b, kv] += dv
+            Dall[b, h] = D
+    return (dQ, dK, dV, Dall) if return_D else (dQ, dK, dV)
+
+
+def ref_forward_rows(q, k, v, b, h, rows, mask=None, scale=None, is_causal=False,
+                     enable_gqa=False):
+    """O and LSE of selected query rows of one (b, h): for sampled checks of large runs.
+
+    Each row is an independent problem (course chapter, section 2.1: every
+    query is computed independently), so a row needs only its own q_i and all
+    keys.
+    """
+    G = q.shape[1] // k.shape[1]
+    kv = h // G
+    rows = np.asarray(rows)
+    L, S, E = q.shape[2], k.shape[2], q.shape[3]
+    alpha = _alpha(scale, E)
+    qh = _as64(q[b, h][rows])
+    kh = _as64(k[b, kv])
+    vh = _as64(v[b, kv])
+    bias = np.zeros((len(rows), S))
+    if mask is not None:
+        m = mask[min(b, mask.shape[0] - 1), min(h, mask.shape[1] - 1)]
+        bias = bias + _as64(m[rows])
+    if is_causal:
+        bias = bias + causal_bias(L, S)[rows]
+    P, lse = _masked_softmax(_scores(qh, kh, alpha), bias)
+    return P @ vh, lse
+
+
+def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False):
+    """Forward and backward of the G query heads sharing KV head (b, kv).
+
+    Returns (O [G,L,Ev], LSE [G,L], dQ [G,L,E], dK [S,E], dV [S,Ev]) for
+    sampled checks of large runs: one KV group is a closed sub-problem.
+    """
+    G = q.shape[1] // k.shape[1]
+    sl = slice(kv * G, (kv + 1) * G)
+    qg = q[b:b + 1, sl]
+    kg = k[b:b + 1, kv:kv + 1]
+    vg = v[b:b + 1, kv:kv + 1]
+    dOg = dO[b:b + 1, sl] if dO is not None else None
+    mg = None
+    if mask is not None:
+        mb = min(b, mask.shape[0] - 1)
+        mg = mask[mb:mb + 1]
+        if mask.shape[1] != 1:
+            mg = mg[:, sl]
+    O, LSE = ref_forward(qg, kg, vg, mg, scale, is_causal, enable_gqa=True)
+    out = [O[0], LSE[0]]
+    if dO is not None:
+        dQ, dK, dV = ref_backward(qg, kg, vg, dOg, mg, scale, is_causal, enable_gqa=True)
+        out += [dQ[0], dK[0, 0], dV[0, 0]]
+    return tuple(out)
