@@ -1,0 +1,156 @@
+/*
+ * sdpa.h - C ABI of a GB300 (sm_103a) scaled dot-product attention library.
+ *
+ * The library computes  O = softmax(alpha * Q K^T + mask) V  (forward, with a
+ * per-row log-sum-exp), its hand-derived backward (dQ, dK, dV), and a
+ * split-KV decode for a single query row.  Definitions follow the course
+ * chapter "Scaled dot-product attention (forward and backward)" (sections 2.1
+ * to 2.3: scores, masked softmax, output, and the backward dV = P^T dO,
+ * dP = dO V^T, dS = P o (dP - D), D = rowsum(dO o O), dQ = alpha dS K,
+ * dK = alpha dS^T Q), the "ScaledDotProductAttentionBackward" API page
+ * (additive mask, engine-side causal j <= i, argument checks), the
+ * "Understanding PyTorch Scaled Dot-Product Attention" post (section 3: causal
+ * = tril(diagonal=0); section 4: grouped-query heads by repeat_interleave) and
+ * the cuDNN "Attention" page (stats = max + ln(sum exp(s - max)), fp32,
+ * natural log; split-KV merges of such statistics).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layout    Every tensor is dense, row-major "BHSD":
+ *              q [B, Hq, L, E]    k [B, Hkv, S, E]    v [B, Hkv, S, Ev]
+ *              o [B, Hq, L, Ev]   dO like o           lse [B, Hq, L] (fp32)
+ *              dq like q          dk like k           dv like v
+ *              mask [mask_b, mask_h, L, S] fp32 with mask_b in {1, B} and
+ *              mask_h in {1, Hq}; a size-1 dimension broadcasts.
+ *  Pointers  All tensor and workspace pointers are DEVICE pointers on the
+ *            current CUDA device, 16-byte aligned.  The caller owns every
+ *            buffer; the library never allocates or frees device memory and
+ *            never synchronises the stream: work is enqueued on `stream`
+ *            (0 = legacy default stream) and the call returns.
+ *  dtype     q, k, v, o, dO, dq, dk, dv share one dtype (SDPA_F32 or
+ *            SDPA_BF16).  mask and lse are always fp32.  Accumulation and all
+ *            softmax statistics are fp32 in every path.
+ *  scale     alpha.  Pass a NaN to select the default 1/sqrt(E).  It scales
+ *            Q K^T only, never the mask.  Negative or infinite -> INVALID_ARG.
+ *  mask      Additive: -inf blocks a (query, key) pair, finite values are
+ *            added to the scaled score.  NULL = no mask.
+ *  causal    is_causal != 0 blocks key j for query i when j > i (top-left
+ *            aligned, for any L and S).  Combines with a mask.
+ *  GQA       Query head h reads KV head h / (Hq / Hkv).  Hq != Hkv requires
+ *            enable_gqa != 0 and Hq % Hkv == 0.  dk and dv are summed over
+ *            the Hq / Hkv query heads that share a KV head.
+ *  Empty rows  A query row whose every key is blocked gets o = 0,
+ *            lse = -inf, dq = 0, and adds nothing to dk, dv.
+ *  Errors    Functions never throw.  Argument errors are detected on the host
+ *            before anything is enqueued.  A kernel launch failure returns
+ *            SDPA_ERR_CUDA.  Kernels never trap: a device-side pipeline wait
+ *            that exceeds its time limit records SDPA_ERR_TIMEOUT in a device
+ *            status word, read by sdpa_last_device_status().
+ *
+ * Supported sizes: B, Hq, Hkv, L, S >= 1.  fp32: 1 <= E, Ev <= 128.  bf16:
+ * E and Ev multiples of 8, at most 128 (the tensor-core prefill and backward
+ * take E, Ev in {64, 128}; other bf16 widths run on the CUDA-core kernels).
+ * Anything else -> SDPA_ERR_UNSUPPORTED.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = 1,   /* bad pointer, shape, scale or workspace size */
+  SDPA_ERR_UNSUPPORTED = 2,   /* valid but outside the supported sizes/dtypes */
+  SDPA_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+  SDPA_ERR_TIMEOUT = 4        /* a device-side wait gave up (see below) */
+} sdpa_status;
+
+typedef enum { SDPA_F32 = 0, SDPA_BF16 = 1 } sdpa_dtype;
+
+/* Problem sizes.  mask_b / mask_h are the mask's first two extents (1 or B,
+ * 1 or Hq); ignored when the mask pointer is NULL. */
+typedef struct {
+  int64_t B, Hq, Hkv, L, S, E, Ev;
+  int32_t dtype;               /* sdpa_dtype */
+  int32_t mask_b, mask_h;
+} sdpa_shape;
+
+/* Forward: o = softmax(scale * q k^T + mask + causal) v and
+ * lse[b,h,i] = max_j t_ij + ln(sum_j exp(t_ij - max_j t_ij)), t = the masked
+ * scaled scores (course chapter sections 2.1-2.2; cuDNN "Attention",
+ * Scaled Dot Product Attention, stats).  lse is always written.
+ * A bf16 call with L == 1, no causal flag and no mask runs the split-KV decode
+ * (same contract as sdpa_decode with num_splits = 0) and needs the workspace
+ * reported by sdpa_forward_workspace_bytes; every other call needs none
+ * (workspace may then be NULL with workspace_bytes = 0). */
+sdpa_status sdpa_forward(const sdpa_shape* shape,
+                         const void* q, const void* k, const void* v,
+                         const float* mask_or_null, double scale,
+                         int is_causal, int enable_gqa,
+                         void* o, float* lse,
+                         void* workspace, size_t workspace_bytes,
+                         void* stream /* cudaStream_t */);
+
+/* Device workspace bytes sdpa_forward needs for `shape` (0 unless the call is
+ * routed to the decode path). */
+size_t sdpa_forward_workspace_bytes(const sdpa_shape* shape);
+
+/* Backward of sum(o * dO) (course chapter section 2.3): writes dq [B,Hq,L,E],
+ * dk [B,Hkv,S,E], dv [B,Hkv,S,Ev].  o and lse must be the forward's outputs for
+ * the same inputs and flags; P is recomputed from q, k and lse, never stored.
+ * D_i = dO_i . o_i is computed in fp32 first.  dq, dk, dv are fully
+ * overwritten.  Needs sdpa_backward_workspace_bytes(shape) bytes of device
+ * workspace (fp32 D, and for bf16 an fp32 dQ accumulator). */
+sdpa_status sdpa_backward(const sdpa_shape* shape,
+                          const void* q, const void* k, const void* v,
+                          const void* o, const void* dO, const float* lse,
+                          const float* mask_or_null, double scale,
+                          int is_causal, int enable_gqa,
+                          void* dq, void* dk, void* dv,
+                          void* workspace, size_t workspace_bytes,
+                          void* stream /* cudaStream_t */);
+
+size_t sdpa_backward_workspace_bytes(const sdpa_shape* shape);
+
+/* Split-KV decode forward (bf16, any L but typically L == 1): the S keys of
+ * each (batch, KV head) are cut into num_splits contiguous ranges; one pass
+ * per range reads its keys and values once for all Hq/Hkv query heads of the
+ * group and writes a partial (o_s, lse_s) to the workspace; a merge pass
+ * combines them: lse = logsumexp_s(lse_s) (empty ranges have lse_s = -inf),
+ * o = sum_s exp(lse_s - lse) o_s (cuDNN "Attention": log-sum-exp statistics
+ * and their split-KV merges).  num_splits = 0 picks a count from the GPU's SM
+ * count.  The result equals the plain forward up to fp32 rounding for every
+ * split count.  No causal flag (it would leave one key for L == 1). */
+sdpa_status sdpa_decode(const sdpa_shape* shape,
+                        const void* q, const void* k, const void* v,
+                        const float* mask_or_null, double scale, int enable_gqa,
+                        int num_splits,
+                        void* o, float* lse,
+                        void* workspace, size_t workspace_bytes,
+                        void* stream /* cudaStream_t */);
+
+/* Workspace bytes for sdpa_decode with this split count (0 = automatic). */
+size_t sdpa_decode_workspace_bytes(const sdpa_shape* shape, int num_splits);
+
+/* The split count sdpa_decode uses for num_splits = 0 on the current device. */
+int sdpa_decode_num_splits(const sdpa_shape* shape);
+
+/* Static, NUL-terminated description of a status code. */
+const char* sdpa_status_string(sdpa_status status);
+
+/* Reads and clears the current device's status word that kernels set when a
+ * bounded device-side wait gives up.  Returns SDPA_OK when no kernel has timed
+ * out since the last call.  Synchronises the device first (call it off the
+ * hot path, e.g. in tests or after an error). */
+sdpa_status sdpa_last_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */

@@ -1,0 +1,244 @@
+"""Python binding of libsdpa_gb300.so (scaled dot-product attention on GB300).
+
+Argument marshalling only: shapes and device pointers of torch tensors are
+passed to the C ABI declared in include/sdpa.h, outputs and workspaces are
+allocated with torch on the inputs' device, and work is enqueued on torch's
+current CUDA stream.  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback.  Importing works without a GPU; calling
+needs the built library (``build()``) and a CUDA device, and raises otherwise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+from .build import LIB_PATH, build  # noqa: F401
+
+__all__ = [
+    "SdpaError", "load_library", "exported_symbols", "sdpa_forward", "sdpa_backward", "sdpa_decode",
+    "forward_workspace_bytes", "backward_workspace_bytes", "decode_workspace_bytes",
+    "decode_num_splits", "last_device_status", "Shape", "build", "LIB_PATH",
+]
+
+SDPA_F32, SDPA_BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout"}
+
+# Every symbol include/sdpa.h declares.
+EXPORTS = (
+    "sdpa_forward", "sdpa_forward_workspace_bytes", "sdpa_backward", "sdpa_backward_workspace_bytes",
+    "sdpa_decode", "sdpa_decode_workspace_bytes", "sdpa_decode_num_splits", "sdpa_status_string",
+    "sdpa_last_device_status",
+)
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} (status {status})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("Hq", ctypes.c_int64), ("Hkv", ctypes.c_int64),
+                ("L", ctypes.c_int64), ("S", ctypes.c_int64), ("E", ctypes.c_int64),
+                ("Ev", ctypes.c_int64), ("dtype", ctypes.c_int32), ("mask_b", ctypes.c_int32),
+                ("mask_h", ctypes.c_int32)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+
+
+def load_library(path: Optional[str] = None):
+    """Load libsdpa_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing; run scaled_dot_product_sm_gb300.build()")
+    lib = ctypes.CDLL(path)
+    SP = ctypes.POINTER(Shape)
+    lib.sdpa_forward.argtypes = [SP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int, _P, _P, _P,
+                                 ctypes.c_size_t, _P]
+    lib.sdpa_forward.restype = ctypes.c_int
+    lib.sdpa_backward.argtypes = [SP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                  _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.sdpa_backward.restype = ctypes.c_int
+    lib.sdpa_decode.argtypes = [SP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int, _P, _P, _P,
+                                ctypes.c_size_t, _P]
+    lib.sdpa_decode.restype = ctypes.c_int
+    for fn in ("sdpa_forward_workspace_bytes", "sdpa_backward_workspace_bytes"):
+        getattr(lib, fn).argtypes = [SP]
+        getattr(lib, fn).restype = ctypes.c_size_t
+    lib.sdpa_decode_workspace_bytes.argtypes = [SP, ctypes.c_int]
+    lib.sdpa_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.sdpa_decode_num_splits.argtypes = [SP]
+    lib.sdpa_decode_num_splits.restype = ctypes.c_int
+    lib.sdpa_status_string.argtypes = [ctypes.c_int]
+    lib.sdpa_status_string.restype = ctypes.c_char_p
+    lib.sdpa_last_device_status.argtypes = []
+    lib.sdpa_last_device_status.restype = ctypes.c_int
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def exported_symbols(path: Optional[str] = None):
+    """Names of EXPORTS that the library resolves (loads it, calls nothing)."""
+    lib = load_library(path)
+    found = []
+    for name in EXPORTS:
+        try:
+            getattr(lib, name)
+            found.append(name)
+        except AttributeError:
+            pass
+    return found
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return SDPA_F32
+    if t.dtype == torch.bfloat16:
+        return SDPA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _shape(q, k, v, mask) -> Shape:
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, T, D]")
+    B, Hq, L, E = q.shape
+    _, Hkv, S, _ = k.shape
+    Ev = v.shape[3]
+    mb, mh = 1, 1
+    if mask is not None:
+        if mask.dim() != 4:
+            raise ValueError("mask must be 4-D [B|1, Hq|1, L, S]")
+        mb, mh = mask.shape[0], mask.shape[1]
+    return Shape(B, Hq, Hkv, L, S, E, Ev, _dtype_code(q), mb, mh)
+
+
+def _check_tensors(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (BHSD)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _scale(scale):
+    return float("nan") if scale is None else float(scale)
+
+
+def _raise(status, where):
+    if status != 0:
+        raise SdpaError(status, where)
+
+
+def _workspace(nbytes, device):
+    import torch
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def forward_workspace_bytes(q, k, v, mask=None) -> int:
+    return int(load_library().sdpa_forward_workspace_bytes(ctypes.byref(_shape(q, k, v, mask))))
+
+
+def backward_workspace_bytes(q, k, v, mask=None) -> int:
+    return int(load_library().sdpa_backward_workspace_bytes(ctypes.byref(_shape(q, k, v, mask))))
+
+
+def decode_workspace_bytes(q, k, v, num_splits=0) -> int:
+    return int(load_library().sdpa_decode_workspace_bytes(ctypes.byref(_shape(q, k, v, None)), int(num_splits)))
+
+
+def decode_num_splits(q, k, v) -> int:
+    return int(load_library().sdpa_decode_num_splits(ctypes.byref(_shape(q, k, v, None))))
+
+
+def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=False,
+                 out=None, lse=None, workspace=None, stream=None):
+    """O [B,Hq,L,Ev] (dtype of q) and LSE [B,Hq,L] fp32 of softmax(scale*q k^T + mask) v."""
+    import torch
+    lib = load_library()
+    _check_tensors(q, k, v, mask)
+    shp = _shape(q, k, v, mask)
+    B, Hq, L, _ = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, L, v.shape[3], dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    need = int(lib.sdpa_forward_workspace_bytes(ctypes.byref(shp)))
+    if workspace is None and need:
+        workspace = _workspace(need, q.device)
+    st = lib.sdpa_forward(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), _scale(scale),
+                          int(bool(is_causal)), int(bool(enable_gqa)), _ptr(out), _ptr(lse), _ptr(workspace),
+                          0 if workspace is None else workspace.numel() * workspace.element_size(),
+                          _stream(stream))
+    _raise(st, "sdpa_forward")
+    return out, lse
+
+
+def sdpa_backward(q, k, v, o, dO, lse, mask=None, scale=None, is_causal=False, enable_gqa=False,
+                  dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sum(O * dO); o and lse are the forward's outputs."""
+    import torch
+    lib = load_library()
+    _check_tensors(q, k, v, o, dO, lse, mask)
+    shp = _shape(q, k, v, mask)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = _workspace(lib.sdpa_backward_workspace_bytes(ctypes.byref(shp)), q.device)
+    st = lib.sdpa_backward(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                           _ptr(mask), _scale(scale), int(bool(is_causal)), int(bool(enable_gqa)), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    _raise(st, "sdpa_backward")
+    return dq, dk, dv
+
+
+def sdpa_decode(q, k, v, mask=None, scale=None, enable_gqa=False, num_splits=0,
+                out=None, lse=None, workspace=None, stream=None):
+    """Split-KV decode forward (bf16): same outputs as sdpa_forward."""
+    import torch
+    lib = load_library()
+    _check_tensors(q, k, v, mask)
+    shp = _shape(q, k, v, mask)
+    B, Hq, L, _ = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, L, v.shape[3], dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(lib.sdpa_decode_workspace_bytes(ctypes.byref(shp), int(num_splits)), q.device)
+    st = lib.sdpa_decode(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), _scale(scale),
+                         int(bool(enable_gqa)), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(st, "sdpa_decode")
+    return out, lse
+
+
+def last_device_status() -> int:
+    """Reads and clears the device status word (synchronises the device)."""
+    return int(load_library().sdpa_last_device_status())
+
+
+def default_scale(E: int) -> float:
+    return 1.0 / math.sqrt(E)

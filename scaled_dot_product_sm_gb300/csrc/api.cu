@@ -1,0 +1,397 @@
+// api.cu - the C ABI declared in include/sdpa.h: argument checks, workspace
+// sizing, routing to the kernels, tensor-map encoding and the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "sdpa.h"
+
+namespace sdpa_impl {
+
+// Written by kernels whose bounded waits give up (see ptx.cuh); read and cleared
+// by sdpa_last_device_status().
+__device__ unsigned g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+unsigned* status_ptr() {
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[d]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[d] = static_cast<unsigned*>(ptr);
+  }
+  return g_status_ptr[d];
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Checked {
+  int B, Hq, Hkv, L, S, E, Ev, G;
+  bool bf16;
+  long long mask_sb, mask_sh;
+};
+
+// Shape checks shared by every entry point; mirrors the argument checks of the
+// "ScaledDotProductAttentionBackward" page (matching batch dims, q/k widths,
+// k/v lengths) plus the grouped-query rule Hq % Hkv == 0.
+sdpa_status check_shape(const sdpa_shape* s, int enable_gqa, bool has_mask, Checked* c) {
+  if (!s) return SDPA_ERR_INVALID_ARG;
+  if (s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->L <= 0 || s->S <= 0 || s->E <= 0 || s->Ev <= 0)
+    return SDPA_ERR_INVALID_ARG;
+  if (s->dtype != SDPA_F32 && s->dtype != SDPA_BF16) return SDPA_ERR_INVALID_ARG;
+  if (s->Hq % s->Hkv != 0) return SDPA_ERR_INVALID_ARG;
+  if (s->Hq != s->Hkv && !enable_gqa) return SDPA_ERR_INVALID_ARG;
+  if (has_mask) {
+    if (!(s->mask_b == 1 || s->mask_b == s->B) || !(s->mask_h == 1 || s->mask_h == s->Hq))
+      return SDPA_ERR_INVALID_ARG;
+  }
+  // sizes the kernels index with 32-bit row counters and grid dimensions
+  if (s->B * s->Hq > INT_MAX || s->L > INT_MAX / 2 || s->S > INT_MAX / 2 || s->B * s->Hkv > 65535 * 64)
+    return SDPA_ERR_UNSUPPORTED;
+  if (s->E > 128 || s->Ev > 128) return SDPA_ERR_UNSUPPORTED;
+  if (s->dtype == SDPA_BF16 && (s->E % 8 != 0 || s->Ev % 8 != 0)) return SDPA_ERR_UNSUPPORTED;
+  c->B = static_cast<int>(s->B);
+  c->Hq = static_cast<int>(s->Hq);
+  c->Hkv = static_cast<int>(s->Hkv);
+  c->L = static_cast<int>(s->L);
+  c->S = static_cast<int>(s->S);
+  c->E = static_cast<int>(s->E);
+  c->Ev = static_cast<int>(s->Ev);
+  c->G = c->Hq / c->Hkv;
+  c->bf16 = s->dtype == SDPA_BF16;
+  const long long LS = s->L * s->S;
+  c->mask_sh = (has_mask && s->mask_h != 1) ? LS : 0;
+  c->mask_sb = (has_mask && s->mask_b != 1) ? LS * s->mask_h : 0;
+  return SDPA_OK;
+}
+
+sdpa_status check_scale(double scale, int E, float* alpha) {
+  if (std::isnan(scale)) {
+    *alpha = static_cast<float>(1.0 / std::sqrt(static_cast<double>(E)));
+    return SDPA_OK;
+  }
+  if (std::isinf(scale) || scale < 0.0) return SDPA_ERR_INVALID_ARG;
+  *alpha = static_cast<float>(scale);
+  return SDPA_OK;
+}
+
+sdpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
+
+void fill_fwd(FwdParams& p, const Checked& c, const void* q, const void* k, const void* v, const float* mask,
+              float alpha, int causal, void* o, float* lse) {
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.mask = mask;
+  p.o = o;
+  p.lse = lse;
+  p.B = c.B;
+  p.Hq = c.Hq;
+  p.Hkv = c.Hkv;
+  p.L = c.L;
+  p.S = c.S;
+  p.E = c.E;
+  p.Ev = c.Ev;
+  p.G = c.G;
+  p.mask_sb = c.mask_sb;
+  p.mask_sh = c.mask_sh;
+  p.scale = alpha;
+  p.scale_log2 = alpha * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.status = status_ptr();
+}
+
+// Split count: at least two waves of (SMs x 2 resident CTAs) and, among up to
+// twice that count, the one whose last wave is fullest.
+int auto_splits(const Checked& c) {
+  const int stage = decode_stage_keys();
+  const long long units =
+      static_cast<long long>(c.B) * c.Hkv * ((c.G * c.L + decode_rows_per_cta() - 1) / decode_rows_per_cta());
+  const long long slots = static_cast<long long>(num_sms()) * 2;
+  const int max_splits = (c.S + stage - 1) / stage;
+  int lo = static_cast<int>((2 * slots + units - 1) / units);
+  lo = std::max(1, std::min(lo, max_splits));
+  int best = lo;
+  double best_eff = -1.0;
+  for (int n = lo; n <= std::min(2 * lo, max_splits); ++n) {
+    const long long ctas = units * n;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double eff = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = n;
+    }
+  }
+  return best;
+}
+
+// Normalises a split count so every split but the last covers a whole number of stages.
+void split_layout(const Checked& c, int want, int* nsplit, int* kps) {
+  const int stage = decode_stage_keys();
+  const int max_splits = (c.S + stage - 1) / stage;
+  want = std::max(1, std::min(want, max_splits));
+  int per = (c.S + want - 1) / want;
+  per = (per + stage - 1) / stage * stage;
+  *kps = per;
+  *nsplit = (c.S + per - 1) / per;
+}
+
+size_t decode_ws(const Checked& c, int nsplit) {
+  const size_t rows = static_cast<size_t>(c.B) * c.Hq * c.L;
+  return round_up(rows * nsplit * c.Ev * sizeof(float), 256) + round_up(rows * nsplit * sizeof(float), 256);
+}
+
+bool routes_to_decode(const Checked& c, bool has_mask, int causal) {
+  (void)has_mask;
+  return c.bf16 && c.L == 1 && !causal && decode_supported(c.E, c.Ev);
+}
+
+size_t bwd_ws(const Checked& c) {
+  const size_t rows = static_cast<size_t>(c.B) * c.Hq * c.L;
+  size_t bytes = round_up(rows * sizeof(float), 256);
+  if (c.bf16 && bwd_tc_supported(c.E, c.Ev)) bytes += round_up(rows * c.E * sizeof(float), 256);
+  return bytes;
+}
+
+sdpa_status run_decode(const Checked& c, const void* q, const void* k, const void* v, const float* mask,
+                       float alpha, int num_splits, void* o, float* lse, void* ws, size_t ws_bytes,
+                       cudaStream_t st) {
+  int nsplit, kps;
+  split_layout(c, num_splits > 0 ? num_splits : auto_splits(c), &nsplit, &kps);
+  if (c.B * c.Hkv * ((c.G * c.L + decode_rows_per_cta() - 1) / decode_rows_per_cta()) > 65535)
+    return SDPA_ERR_UNSUPPORTED;
+  const size_t need = decode_ws(c, nsplit);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return SDPA_ERR_INVALID_ARG;
+  DecodeParams dp;
+  fill_fwd(dp.f, c, q, k, v, mask, alpha, 0, o, lse);
+  const size_t rows = static_cast<size_t>(c.B) * c.Hq * c.L;
+  dp.part_o = static_cast<float*>(ws);
+  dp.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                         round_up(rows * nsplit * c.Ev * sizeof(float), 256));
+  dp.nsplit = nsplit;
+  dp.keys_per_split = kps;
+  return from_cuda(launch_decode(dp, st));
+}
+
+}  // namespace
+
+int num_sms() {
+  const int d = current_device();
+  if (d < 0) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[d]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 148;
+    g_sms[d] = n;
+  }
+  return g_sms[d];
+}
+
+bool encode_tmap_bf16_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                         uint32_t box1) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode_tried) {
+      g_encode_tried = true;
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+              cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  if (!g_encode) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace sdpa_impl
+
+using namespace sdpa_impl;
+
+extern "C" {
+
+sdpa_status sdpa_forward(const sdpa_shape* shape, const void* q, const void* k, const void* v,
+                         const float* mask_or_null, double scale, int is_causal, int enable_gqa, void* o,
+                         float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  Checked c;
+  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
+  if (s != SDPA_OK) return s;
+  float alpha;
+  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (mask_or_null && !aligned16(mask_or_null)))
+    return SDPA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (routes_to_decode(c, mask_or_null != nullptr, is_causal))
+    return run_decode(c, q, k, v, mask_or_null, alpha, 0, o, lse, workspace, workspace_bytes, st);
+  FwdParams p;
+  fill_fwd(p, c, q, k, v, mask_or_null, alpha, is_causal, o, lse);
+  if (c.bf16 && fwd_tc_supported(c.E, c.Ev)) {
+    if ((c.L + 255) / 256 > 65535) return SDPA_ERR_UNSUPPORTED;
+    return from_cuda(launch_fwd_tc(p, st));
+  }
+  if ((c.L + 15) / 16 > 65535 || static_cast<long long>(c.B) * c.Hq > 65535) return SDPA_ERR_UNSUPPORTED;
+  return from_cuda(launch_fwd_simt(p, c.bf16 ? 1 : 0, st));
+}
+
+size_t sdpa_forward_workspace_bytes(const sdpa_shape* shape) {
+  Checked c;
+  if (check_shape(shape, 1, false, &c) != SDPA_OK) return 0;
+  if (!routes_to_decode(c, false, 0)) return 0;
+  int nsplit, kps;
+  split_layout(c, auto_splits(c), &nsplit, &kps);
+  return decode_ws(c, nsplit);
+}
+
+sdpa_status sdpa_decode(const sdpa_shape* shape, const void* q, const void* k, const void* v,
+                        const float* mask_or_null, double scale, int enable_gqa, int num_splits, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  Checked c;
+  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
+  if (s != SDPA_OK) return s;
+  float alpha;
+  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
+  if (num_splits < 0) return SDPA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (mask_or_null && !aligned16(mask_or_null)))
+    return SDPA_ERR_INVALID_ARG;
+  if (!c.bf16 || !decode_supported(c.E, c.Ev)) return SDPA_ERR_UNSUPPORTED;
+  return run_decode(c, q, k, v, mask_or_null, alpha, num_splits, o, lse, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+size_t sdpa_decode_workspace_bytes(const sdpa_shape* shape, int num_splits) {
+  Checked c;
+  if (check_shape(shape, 1, false, &c) != SDPA_OK || num_splits < 0) return 0;
+  int nsplit, kps;
+  split_layout(c, num_splits > 0 ? num_splits : auto_splits(c), &nsplit, &kps);
+  return decode_ws(c, nsplit);
+}
+
+int sdpa_decode_num_splits(const sdpa_shape* shape) {
+  Checked c;
+  if (check_shape(shape, 1, false, &c) != SDPA_OK) return 0;
+  int nsplit, kps;
+  split_layout(c, auto_splits(c), &nsplit, &kps);
+  return nsplit;
+}
+
+sdpa_status sdpa_backward(const sdpa_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, const float* mask_or_null, double scale,
+                          int is_causal, int enable_gqa, void* dq, void* dk, void* dv, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  Checked c;
+  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
+  if (s != SDPA_OK) return s;
+  float alpha;
+  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return SDPA_ERR_INVALID_ARG;
+  if (mask_or_null && !aligned16(mask_or_null)) return SDPA_ERR_INVALID_ARG;
+  const size_t need = bwd_ws(c);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SDPA_ERR_INVALID_ARG;
+  BwdParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dO = dO;
+  p.lse = lse;
+  p.mask = mask_or_null;
+  const size_t rows = static_cast<size_t>(c.B) * c.Hq * c.L;
+  p.D = static_cast<float*>(workspace);
+  p.dq_acc = (c.bf16 && bwd_tc_supported(c.E, c.Ev))
+                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float), 256))
+                 : nullptr;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = c.B;
+  p.Hq = c.Hq;
+  p.Hkv = c.Hkv;
+  p.L = c.L;
+  p.S = c.S;
+  p.E = c.E;
+  p.Ev = c.Ev;
+  p.G = c.G;
+  p.mask_sb = c.mask_sb;
+  p.mask_sh = c.mask_sh;
+  p.scale = alpha;
+  p.scale_log2 = alpha * kLog2e;
+  p.causal = is_causal ? 1 : 0;
+  p.status = status_ptr();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_preprocess(p, c.bf16 ? 1 : 0, st);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  if (p.dq_acc) return from_cuda(launch_bwd_tc(p, st));
+  if ((c.L + 15) / 16 > 65535 || (c.S + 15) / 16 > 65535 || static_cast<long long>(c.B) * c.Hq > 65535)
+    return SDPA_ERR_UNSUPPORTED;
+  return from_cuda(launch_bwd_simt(p, c.bf16 ? 1 : 0, st));
+}
+
+size_t sdpa_backward_workspace_bytes(const sdpa_shape* shape) {
+  Checked c;
+  if (check_shape(shape, 1, false, &c) != SDPA_OK) return 0;
+  return bwd_ws(c);
+}
+
+const char* sdpa_status_string(sdpa_status status) {
+  switch (status) {
+    case SDPA_OK: return "ok";
+    case SDPA_ERR_INVALID_ARG: return "invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case SDPA_ERR_CUDA: return "CUDA error";
+    case SDPA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+sdpa_status sdpa_last_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return SDPA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return SDPA_ERR_CUDA;
+    return static_cast<sdpa_status>(v & 0xffu);
+  }
+  return SDPA_OK;
+}
+
+}  // extern "C"

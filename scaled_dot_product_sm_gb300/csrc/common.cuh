@@ -1,0 +1,104 @@
+// common.cuh - parameter blocks and small device helpers shared by the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace sdpa_impl {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status codes written by bounded waits: low byte = sdpa_status value
+// (4 = timeout), next byte = which wait gave up (for diagnosis).
+constexpr unsigned kStatusTimeout = 4u;
+__host__ __device__ constexpr unsigned status_code(unsigned where) { return kStatusTimeout | (where << 8); }
+
+// Forward problem (prefill and decode).  Strides are in elements.
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* mask;     // nullptr or [mask_b, mask_h, L, S]
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, L, S, E, Ev, G;
+  long long mask_sb;     // element stride of the mask's batch index (0 when broadcast)
+  long long mask_sh;     // element stride of the mask's head index (0 when broadcast)
+  float scale;           // alpha
+  float scale_log2;      // alpha * log2(e)
+  int causal;
+  unsigned* status;
+};
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dO;
+  const float* lse;
+  const float* mask;
+  float* D;              // [B, Hq, L] fp32 workspace
+  float* dq_acc;         // [B, Hq, L, E] fp32 workspace (bf16 tensor-core path) or nullptr
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, Hq, Hkv, L, S, E, Ev, G;
+  long long mask_sb, mask_sh;
+  float scale, scale_log2;
+  int causal;
+  unsigned* status;
+};
+
+struct DecodeParams {
+  FwdParams f;
+  float* part_o;         // [B*Hq*L, nsplit, Ev] fp32: normalised partial outputs
+  float* part_lse;       // [B*Hq*L, nsplit]     fp32: partial log2-sum-exp (log2 units)
+  int nsplit;
+  int keys_per_split;    // multiple of the decode stage
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Pack two floats into a bf16x2 word (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- host launchers
+cudaError_t launch_fwd_simt(const FwdParams& p, int is_bf16, cudaStream_t st);
+cudaError_t launch_bwd_simt(const BwdParams& p, int is_bf16, cudaStream_t st);
+cudaError_t launch_bwd_preprocess(const BwdParams& p, int is_bf16, cudaStream_t st);
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+bool fwd_tc_supported(int E, int Ev);
+bool bwd_tc_supported(int E, int Ev);
+bool decode_supported(int E, int Ev);
+int decode_rows_per_cta();
+int decode_stage_keys();
+
+// Tensor-map encoder obtained from the driver at run time (no libcuda link).
+bool encode_tmap_bf16_3d(void* tmap /* CUtensorMap* */, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint32_t box0, uint32_t box1);
+int num_sms();
+
+}  // namespace sdpa_impl

@@ -1,0 +1,383 @@
+// fwd_tc.cu - bf16 prefill forward on the 5th-generation tensor cores.
+//
+// O = softmax(alpha Q K^T + mask + causal) V with a per-row log-sum-exp
+// (course chapter "Scaled dot-product attention (forward and backward)",
+// sections 2.1-2.2; stats as on the cuDNN "Attention" page), computed one
+// 128-key tile at a time with a running max and sum (online softmax).
+//
+// One CTA = one (batch, query head) and two 128-row query tiles (256 rows)
+// that share every K/V tile load.  Warp roles (320 threads):
+//   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax of query tile 1
+//   warp  8    TMA producer: Q tiles once, then K_j, V_j through an NS-stage ring
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+Ev), O_1 [384,384+Ev).
+// The MMA issue order per key tile j is  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1),
+// so the tensor core works on one query tile while the other tile's softmax
+// runs.  A commit after S_t(j+1) also covers PV_t(j), so when the softmax of
+// tile t sees S_t(j+1) ready, O_t is complete and its P buffer is free.
+// P goes to shared memory as bf16 in the 128-byte-swizzled K-major layout the
+// MMA reads.  Exponentials are exp2 with alpha*log2(e) folded into the scale;
+// O is only rescaled when a row's max grows by more than 2^8 (the stale max
+// keeps every p below 256, and O/l is exact either way).
+// Causal: key tiles entirely above the diagonal are neither loaded nor
+// computed; only tiles that cross it test j <= i per element.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sdpa_impl {
+
+namespace {
+
+using namespace sdpa_ptx;
+
+constexpr int BM = 128;        // query rows per tile (MMA M)
+constexpr int BN = 128;        // keys per tile (MMA N of S, K of PV)
+constexpr int kThreads = 320;
+constexpr int kChunkBytes = 128 * 128;   // one [128 rows x 64 bf16] swizzled block
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int ECH, int VCH>
+struct FwdCfg {
+  static constexpr int E = ECH * 64, Ev = VCH * 64;
+  static constexpr int kQBytes = ECH * kChunkBytes;                          // one query tile
+  static constexpr int kItem = (ECH > VCH ? ECH : VCH) * kChunkBytes;       // one K or V tile
+  static constexpr int kPBytes = 2 * kChunkBytes;                            // 128 x 128 bf16
+  static constexpr int kFixed = 2 * kQBytes + 2 * kPBytes;
+  static constexpr int kBudget = 227 * 1024 - 2048;
+  static constexpr int NS = (kBudget - kFixed) / kItem > 8 ? 8 : (kBudget - kFixed) / kItem;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;
+  static constexpr int kOffRing = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffRing + NS * kItem;
+  static constexpr int kBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
+  static_assert(NS >= 2, "not enough shared memory for a 2-stage ring");
+};
+
+template <int ECH, int VCH>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, FwdParams p) {
+  using C = FwdCfg<ECH, VCH>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* bar_q = bar;                 // 1
+  uint64_t* full = bar + 1;              // NS
+  uint64_t* empty = full + NS;           // NS
+  uint64_t* s_full = empty + NS;         // 2
+  uint64_t* p_full = s_full + 2;         // 2
+  uint64_t* o_final = p_full + 2;        // 2
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x, b = bh / p.Hq, h = bh - b * p.Hq;
+  const int bkv = b * p.Hkv + h / p.G;
+  const int unit = gridDim.y - 1 - blockIdx.y;      // longest (causal) units first
+  const int r0 = unit * 2 * BM;
+  int n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rt = r0 + t * BM;
+    if (rt >= p.L) {
+      n_t[t] = 0;
+    } else {
+      const int kmax = p.causal ? min(p.S, rt + BM) : p.S;
+      n_t[t] = (kmax + BN - 1) / BN;
+    }
+  }
+  const int n = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], BM);
+      mbar_init(&o_final[t], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const int nq = (n_t[0] > 0) + (n_t[1] > 0);
+      mbar_arrive_expect_tx(bar_q, nq * C::kQBytes);
+      for (int t = 0; t < 2; ++t) {
+        if (n_t[t] == 0) continue;
+        for (int c = 0; c < ECH; ++c)
+          tma_load_3d(smem + C::kOffQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar_q, c * 64, r0 + t * BM, bh);
+      }
+      int it = 0;
+      for (int j = 0; j < n; ++j) {
+        for (int kv = 0; kv < 2; ++kv, ++it) {
+          const int s = it % NS;
+          mbar_wait(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.status, status_code(0x11));
+          uint8_t* dst = smem + C::kOffRing + s * C::kItem;
+          const int ch = kv == 0 ? ECH : VCH;
+          mbar_arrive_expect_tx(&full[s], ch * kChunkBytes);
+          for (int c = 0; c < ch; ++c)
+            tma_load_3d(dst + c * kChunkBytes, kv == 0 ? &tmK : &tmV, &full[s], c * 64, j * BN, bkv);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);        // Q (K-major) x K (K-major)
+      constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (K-major) x V (MN-major)
+      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
+      const uint32_t p_addr = smem_u32(smem + C::kOffP);
+      const uint32_t ring = smem_u32(smem + C::kOffRing);
+      auto issue_s = [&](int t, uint32_t kaddr) {
+        const uint32_t qa = q_addr + t * C::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::E / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          umma_ss(tmem + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024), idesc_s,
+                  kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+        const uint32_t pa = p_addr + t * C::kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          umma_ss(tmem + 256 + t * 128, sdesc_sw128(pa + aoff, 16, 1024),
+                  sdesc_sw128(vaddr + kk * 16 * 128, kChunkBytes, 1024), idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      mbar_wait(bar_q, 0, abort_flag, p.status, status_code(0x12));
+      int it = 0;
+      // S_t(0)
+      {
+        const int s = it % NS;
+        mbar_wait(&full[s], (it / NS) & 1, abort_flag, p.status, status_code(0x13));
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (n_t[t] == 0) continue;
+          issue_s(t, ring + s * C::kItem);
+          umma_commit(&s_full[t]);
+        }
+        umma_commit(&empty[s]);
+        ++it;
+      }
+      for (int j = 0; j < n; ++j) {
+        const int sv = it % NS;
+        mbar_wait(&full[sv], (it / NS) & 1, abort_flag, p.status, status_code(0x14));
+        tc_fence_after();
+        ++it;
+        int sk = -1;
+        for (int t = 0; t < 2; ++t) {
+          if (j >= n_t[t]) continue;
+          mbar_wait(&p_full[t], j & 1, abort_flag, p.status, status_code(0x15));
+          tc_fence_after();
+          issue_pv(t, ring + sv * C::kItem, j > 0);
+          if (j + 1 < n_t[t]) {
+            if (sk < 0) {
+              sk = it % NS;
+              mbar_wait(&full[sk], (it / NS) & 1, abort_flag, p.status, status_code(0x16));
+              tc_fence_after();
+              ++it;
+            }
+            issue_s(t, ring + sk * C::kItem);
+            umma_commit(&s_full[t]);
+          } else {
+            umma_commit(&o_final[t]);
+          }
+        }
+        umma_commit(&empty[sv]);
+        if (sk >= 0) umma_commit(&empty[sk]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int t = warp >> 2;               // query tile
+    const int wq = warp & 3;               // TMEM lane quarter
+    const int r = wq * 32 + lane;          // row within the tile = TMEM lane
+    const int row = r0 + t * BM + r;
+    const int nt = n_t[t];
+    if (nt > 0) {
+      const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t tS = tmem + lane_off + t * BN;
+      const uint32_t tO = tmem + lane_off + 256 + t * 128;
+      uint8_t* prow = smem + C::kOffP + t * C::kPBytes + r * 128;
+      const float* mrow = (p.mask && row < p.L)
+                              ? p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(row) * p.S
+                              : nullptr;
+      const int row_first = r0 + t * BM;   // first row of this tile
+      float m_run = kNegInf, l_run = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        mbar_wait(&s_full[t], j & 1, abort_flag, p.status, status_code(0x17));
+        tc_fence_after();
+        float x[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(v[i]) * p.scale_log2;
+        }
+        const int kb = j * BN;
+        if (mrow) {
+          if ((p.S & 3) == 0) {
+            // rows start on 16-byte boundaries only when S is a multiple of 4
+#pragma unroll
+            for (int c = 0; c < BN / 4; ++c) {
+              const int key = kb + 4 * c;
+              if (key < p.S) {
+                const float4 mv = __ldg(reinterpret_cast<const float4*>(mrow + key));
+                x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
+                x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
+                x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
+                x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (kb + i < p.S) x[i] = fmaf(__ldg(mrow + kb + i), kLog2e, x[i]);
+          }
+        }
+        if (kb + BN > p.S) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (kb + i >= p.S) x[i] = kNegInf;
+        }
+        if (p.causal && kb + BN - 1 > row_first) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (kb + i > row) x[i] = kNegInf;
+        }
+        float mx = x[0];
+#pragma unroll
+        for (int i = 1; i < BN; ++i) mx = fmaxf(mx, x[i]);
+        const float m_new = fmaxf(m_run, mx);
+        const bool need = m_new > m_run + kRescaleThreshold;
+        const float m_use = need ? m_new : m_run;
+        const float msafe = (m_use == kNegInf) ? 0.f : m_use;
+        const float corr = need ? ex2(m_run - msafe) : 1.f;
+        // p = exp2(x - m), row sum, bf16 P into the swizzled smem tile
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN / 8; ++c) {
+          float pv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            pv[u] = ex2(x[c * 8 + u] - msafe);
+            rs += pv[u];
+          }
+          uint4 w;
+          w.x = pack_bf16x2(pv[0], pv[1]);
+          w.y = pack_bf16x2(pv[2], pv[3]);
+          w.z = pack_bf16x2(pv[4], pv[5]);
+          w.w = pack_bf16x2(pv[6], pv[7]);
+          const int chunk = c & 7, half = c >> 3;
+          *reinterpret_cast<uint4*>(prow + half * kChunkBytes + ((chunk ^ (r & 7)) << 4)) = w;
+        }
+        l_run = l_run * corr + rs;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c = 0; c < C::Ev / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+            tmem_st32(tO + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+        m_run = m_use;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+      }
+      // ---------------------------------------------------------- epilogue
+      mbar_wait(&o_final[t], 0, abort_flag, p.status, status_code(0x18));
+      tc_fence_after();
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.L + row) * C::Ev;
+#pragma unroll
+      for (int c = 0; c < C::Ev / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + c * 32, v);
+        if (row < p.L) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[u * 8 + 0]) * inv, __uint_as_float(v[u * 8 + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(v[u * 8 + 2]) * inv, __uint_as_float(v[u * 8 + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(v[u * 8 + 4]) * inv, __uint_as_float(v[u * 8 + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(v[u * 8 + 6]) * inv, __uint_as_float(v[u * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) = w;
+          }
+        }
+      }
+      if (row < p.L)
+        p.lse[static_cast<size_t>(bh) * p.L + row] = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int ECH, int VCH>
+cudaError_t run(const FwdParams& p, cudaStream_t st) {
+  using C = FwdCfg<ECH, VCH>;
+  alignas(64) CUtensorMap tmQ, tmK, tmV;
+  if (!encode_tmap_bf16_3d(&tmQ, p.q, C::E, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BM) ||
+      !encode_tmap_bf16_3d(&tmK, p.k, C::E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BN) ||
+      !encode_tmap_bf16_3d(&tmV, p.v, C::Ev, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BN))
+    return cudaErrorInvalidValue;
+  auto kern = fwd_tc_kernel<ECH, VCH>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.B * p.Hq, (p.L + 2 * BM - 1) / (2 * BM));
+  kern<<<grid, kThreads, C::kBytes, st>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fwd_tc_supported(int E, int Ev) { return (E == 64 || E == 128) && (Ev == 64 || Ev == 128); }
+
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t st) {
+  const int ech = p.E / 64, vch = p.Ev / 64;
+  if (ech == 2 && vch == 2) return run<2, 2>(p, st);
+  if (ech == 1 && vch == 1) return run<1, 1>(p, st);
+  if (ech == 2 && vch == 1) return run<2, 1>(p, st);
+  return run<1, 2>(p, st);
+}
+
+}  // namespace sdpa_impl

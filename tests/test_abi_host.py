@@ -1,0 +1,144 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must build (or be built), load, and export every function that
+include/sdpa.h declares.  Argument validation happens on the host before any
+launch, so invalid calls are exercised here with pointers that are never
+dereferenced: every call below is rejected by a check, none reaches a kernel.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import scaled_dot_product_sm_gb300 as sdpa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sdpa.build()
+    return sdpa.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(sdpa_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_exported_list():
+    assert header_functions() == sorted(sdpa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    assert sdpa.exported_symbols() == list(sdpa.EXPORTS)
+    for name in header_functions():
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.sdpa_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.sdpa_status_string(99) == b"unknown status"
+
+
+def _shape(B=1, Hq=2, Hkv=2, L=8, S=8, E=64, Ev=64, dtype=1, mb=1, mh=1):
+    return sdpa.Shape(B, Hq, Hkv, L, S, E, Ev, dtype, mb, mh)
+
+
+FAKE = 1 << 20           # 16-byte aligned; never dereferenced (every call below fails validation)
+P = ctypes.c_void_p
+
+
+def _fwd(lib, shp, q=FAKE, k=FAKE, v=FAKE, mask=None, scale=float("nan"), causal=0, gqa=0, o=FAKE, lse=FAKE):
+    return lib.sdpa_forward(ctypes.byref(shp), P(q), P(k), P(v), P(mask), scale, causal, gqa, P(o), P(lse),
+                            None, 0, None)
+
+
+def _bwd(lib, shp, ws=FAKE, wsb=0, scale=float("nan"), gqa=0, dq=FAKE):
+    return lib.sdpa_backward(ctypes.byref(shp), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None,
+                             scale, 0, gqa, P(dq), P(FAKE), P(FAKE), P(ws), wsb, None)
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(L=0), dict(S=-1), dict(E=0), dict(Ev=0), dict(dtype=7),
+                                dict(Hq=3, Hkv=2)])
+def test_forward_rejects_bad_shapes(lib, kw):
+    assert _fwd(lib, _shape(**kw), gqa=1) == INVALID
+
+
+def test_forward_rejects_gqa_without_flag(lib):
+    assert _fwd(lib, _shape(Hq=4, Hkv=2), gqa=0) == INVALID
+
+
+def test_forward_rejects_bad_mask_dims(lib):
+    assert _fwd(lib, _shape(B=2, mb=3), mask=FAKE) == INVALID
+    assert _fwd(lib, _shape(Hq=2, mh=4), mask=FAKE) == INVALID
+
+
+@pytest.mark.parametrize("scale", [-1.0, float("inf"), float("-inf")])
+def test_forward_rejects_bad_scale(lib, scale):
+    assert _fwd(lib, _shape(), scale=scale) == INVALID
+
+
+def test_forward_rejects_null_and_misaligned(lib):
+    assert _fwd(lib, _shape(), q=0) == INVALID
+    assert _fwd(lib, _shape(), lse=0) == INVALID
+    assert _fwd(lib, _shape(), k=FAKE + 4) == INVALID
+    assert _fwd(lib, _shape(), mask=FAKE + 8) == INVALID
+
+
+def test_forward_rejects_unsupported_sizes(lib):
+    assert _fwd(lib, _shape(E=256, Ev=256)) == UNSUPPORTED
+    assert _fwd(lib, _shape(E=60)) == UNSUPPORTED          # bf16 widths must be multiples of 8
+
+
+def test_backward_rejects_small_workspace(lib):
+    shp = _shape()
+    need = lib.sdpa_backward_workspace_bytes(ctypes.byref(shp))
+    assert need >= 2 * 8 * 4
+    assert _bwd(lib, shp, ws=FAKE, wsb=need - 1) == INVALID
+    assert _bwd(lib, shp, ws=0, wsb=need) == INVALID
+    assert _bwd(lib, shp, ws=FAKE, wsb=need, dq=0) == INVALID
+    assert _bwd(lib, shp, ws=FAKE, wsb=need, scale=-2.0) == INVALID
+
+
+def test_decode_workspace_and_splits(lib):
+    shp = _shape(B=16, Hq=32, Hkv=8, L=1, S=32768, E=128, Ev=128)
+    n = lib.sdpa_decode_num_splits(ctypes.byref(shp))
+    assert 1 <= n <= 32768 // 64
+    for splits in (1, 2, 7):
+        ws = lib.sdpa_decode_workspace_bytes(ctypes.byref(shp), splits)
+        rows = 16 * 32
+        assert ws >= rows * splits * (128 + 1) * 4
+    assert lib.sdpa_forward_workspace_bytes(ctypes.byref(shp)) == lib.sdpa_decode_workspace_bytes(
+        ctypes.byref(shp), 0)
+    # prefill needs no forward workspace
+    assert lib.sdpa_forward_workspace_bytes(ctypes.byref(_shape(L=64))) == 0
+    # decode rejects a negative split count and a too-small workspace before launching
+    st = lib.sdpa_decode(ctypes.byref(shp), P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 1, -1, P(FAKE),
+                         P(FAKE), P(FAKE), 1 << 30, None)
+    assert st == INVALID
+    st = lib.sdpa_decode(ctypes.byref(shp), P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 1, 4, P(FAKE),
+                         P(FAKE), P(FAKE), 16, None)
+    assert st == INVALID
+
+
+def test_backward_workspace_size_formula(lib):
+    shp = _shape(B=2, Hq=4, Hkv=2, L=100, S=50, E=64, Ev=64, dtype=0)
+    # fp32: D only, rounded to 256 bytes
+    assert lib.sdpa_backward_workspace_bytes(ctypes.byref(shp)) == (2 * 4 * 100 * 4 + 255) // 256 * 256
+
+
+def test_binding_requires_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 8)
+    with pytest.raises(ValueError):
+        sdpa.sdpa_forward(q, q, q)
