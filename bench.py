@@ -1,0 +1,540 @@
+"""Benchmark of the GB300 scaled dot-product attention library.
+
+One step = one forward (O and LSE) plus one backward (dQ, dK, dV) of the
+LLaMA-style grouped-query causal workload (B=2, Hq=32, Hkv=8, L=S=4096,
+E=Ev=128, bf16), inputs already resident in HBM.  Metric: TFLOP/s with the
+nominal FLOP counts 4*B*Hq*L*S*E (forward) and 10*B*Hq*L*S*E (backward),
+halved for causal.  In the same run a second leg times the memory-bound
+split-KV decode (B=16, Hq=32, Hkv=8, one query token, S=32768, bf16) in HBM
+GB/s of K and V read once.
+
+Timing: W warm-up steps, then K steps each bracketed by CUDA events on the
+launching stream, with a 256 MiB L2 flush between steps outside the events;
+a barrier and a device synchronize on both sides of the timed loop; the max
+over ranks.  nvidia-smi clocks are sampled during the timed loop.  "e2e" is
+the same step through the same calls with host (pinned) buffers: inputs copied
+host->device and every output copied device->host inside the timed region.
+
+--impl reference times the float64 CPU oracle (the parity reference, not a
+tuned CPU implementation) on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
+GPU with no data exchange (weak scaling); value = all ranks' FLOPs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SDPA fwd/bwd TFLOP/s and % of GB300 bf16 peak; decode HBM GB/s"
+MAIN = "gqa_causal_e128"
+DECODE = "gqa_decode_s32k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--phase", choices=["all", "fwd", "decode"], default="all",
+                    help="profiling aid: run only the forward loop or only the decode leg")
+    ap.add_argument("--summarize-launches", metavar="CSV",
+                    help="print a per-kernel summary of an ncu launch list (gpu__time_duration.sum, --csv) and exit")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    args.steps = max(1, args.steps)
+    return args
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "sm_max_mhz")}, \
+            "measured"
+    except Exception:  # noqa: BLE001
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ helpers
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "scaled_dot_product_sm_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, sources):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel)
+        if ent and ent.get("source_sha") == source_sha(*sources):
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:  # noqa: BLE001
+        pass
+    return None
+
+
+def fp32_alu_peak_tflops(sms: int, mhz: float) -> float:
+    """FFMA peak: SMs x 128 fp32 lanes x 2 flops x clock."""
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import scaled_dot_product_sm_gb300 as sdpa
+    import workloads
+
+    torch.cuda.set_device(local)
+    sdpa.build()
+    sdpa.load_library()
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+
+    w = workloads.get(MAIN)
+    q_h, k_h, v_h, dO_h, _ = workloads.make_inputs(w, seed=0)
+    host = [t.pin_memory() for t in (q_h, k_h, v_h, dO_h)]
+    q, k, v, dO = (t.to(dev) for t in host)
+    scale = w.scale
+    stream = torch.cuda.current_stream()
+    o = torch.empty(w.B, w.Hq, w.L, w.Ev, dtype=q.dtype, device=dev)
+    lse = torch.empty(w.B, w.Hq, w.L, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(max(16, sdpa.backward_workspace_bytes(q, k, v)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        sdpa.sdpa_forward(q, k, v, None, scale, w.is_causal, w.enable_gqa, out=o, lse=lse)
+
+    def bwd():
+        sdpa.sdpa_backward(q, k, v, o, dO, lse, None, scale, w.is_causal, w.enable_gqa, dq=dq, dk=dk, dv=dv,
+                           workspace=bws)
+
+    if args.phase == "decode":
+        return run_decode_only(args, ws, local, dev, peaks)
+    fwd_only = args.phase == "fwd"
+    for _ in range(args.warmup):
+        fwd()
+        if not fwd_only:
+            bwd()
+    torch.cuda.synchronize()
+    assert sdpa.last_device_status() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            fwd()
+            evs[i][1].record(stream)
+            if not fwd_only:
+                bwd()
+            evs[i][2].record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    clocks = clk.summary()
+    t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    t_step = t_fwd + t_bwd
+    t_step_max = reduce_max(t_step, ws)
+    f_fwd, f_bwd = w.flops("fwd"), w.flops("bwd")
+    value = ws * (f_fwd + f_bwd) / (t_step_max * 1e-3) / 1e12
+    assert sdpa.last_device_status() == 0
+
+    # ---------------------------------------------------------- end to end (host buffers)
+    if fwd_only:
+        return {"phase": "fwd", "ms": round(t_fwd, 4), "tflops": round(f_fwd / (t_fwd * 1e-3) / 1e12, 2)}
+    e2e = None
+    if not args.no_e2e:
+        out_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+        h2d = sum(t.numel() * t.element_size() for t in host)
+        d2h = sum(t.numel() * t.element_size() for t in out_h)
+
+        def e2e_step():
+            for src, dst in zip(host, (q, k, v, dO)):
+                dst.copy_(src, non_blocking=True)
+            fwd()
+            bwd()
+            for src, dst in zip((o, lse, dq, dk, dv), out_h):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        t_e2e = reduce_max(e0.elapsed_time(e1) / args.steps, ws)
+        e2e = {"value": round(ws * (f_fwd + f_bwd) / (t_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---------------------------------------------------------- launches and roofline
+    bwd_tc = sdpa.backward_workspace_bytes(q, k, v) > 4 * w.B * w.Hq * w.L + 256
+    bwd_launches = 3
+    fwd_launches = 1
+    launches = args.steps * (fwd_launches + bwd_launches)
+    phases = {
+        "fwd": {"ms": round(t_fwd, 4), "tflops": round(f_fwd / (t_fwd * 1e-3) / 1e12, 2),
+                "frac_of_bf16_peak": round(f_fwd / (t_fwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "kernel": "fwd_tc_kernel", "launches_per_step": fwd_launches},
+        "bwd": {"ms": round(t_bwd, 4), "tflops": round(f_bwd / (t_bwd * 1e-3) / 1e12, 2),
+                "frac_of_bf16_peak": round(f_bwd / (t_bwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "kernel": "bwd_tc_kernel" if bwd_tc else "bwd_dq_simt_kernel+bwd_dkdv_simt_kernel",
+                "launches_per_step": bwd_launches},
+    }
+    if t_fwd >= t_bwd:
+        achieved = f_fwd / (t_fwd * 1e-3) / 1e12
+        roof = {"kernel": "fwd_tc_kernel", "bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic_for("fwd_tc_kernel", ["fwd_tc.cu", "ptx.cuh", "common.cuh"]),
+                "peak_source": f"{peak_src} bf16 dense burst",
+                "algorithmic_per_launch": f_fwd}
+    else:
+        achieved = f_bwd / (t_bwd * 1e-3) / 1e12
+        if bwd_tc:
+            roof = {"kernel": "bwd_tc_kernel", "bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "traffic": traffic_for("bwd_tc_kernel", ["bwd_tc.cu", "ptx.cuh", "common.cuh"]),
+                    "peak_source": f"{peak_src} bf16 dense burst", "algorithmic_per_launch": f_bwd}
+        else:
+            pk = fp32_alu_peak_tflops(sms, peaks["sm_max_mhz"])
+            roof = {"kernel": "bwd_dq_simt_kernel+bwd_dkdv_simt_kernel", "bound": "alu",
+                    "achieved": round(achieved, 2), "peak": round(pk, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / pk, 4), "traffic": None,
+                    "peak_source": f"FFMA: {sms} SMs x 128 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                    "algorithmic_per_launch": f_bwd}
+    roof["duration_ms"] = round(max(t_fwd, t_bwd), 4)
+
+    # ---------------------------------------------------------- decode leg
+    decode = None
+    if not args.no_decode:
+        del flush
+        wd = workloads.get(DECODE)
+        qd_h, kd_h, vd_h, _, _ = workloads.make_inputs(wd, seed=0, with_grad=False)
+        qd, kd, vd = qd_h.to(dev), kd_h.to(dev), vd_h.to(dev)
+        del qd_h, kd_h, vd_h
+        od = torch.empty(wd.B, wd.Hq, 1, wd.Ev, dtype=qd.dtype, device=dev)
+        lsed = torch.empty(wd.B, wd.Hq, 1, dtype=torch.float32, device=dev)
+        dws = torch.empty(max(16, sdpa.decode_workspace_bytes(qd, kd, vd, 0)), dtype=torch.uint8, device=dev)
+        nsplit = sdpa.decode_num_splits(qd, kd, vd)
+
+        def dstep():
+            sdpa.sdpa_decode(qd, kd, vd, None, wd.scale, True, 0, out=od, lse=lsed, workspace=dws)
+
+        for _ in range(args.warmup):
+            dstep()
+        torch.cuda.synchronize()
+        dev_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+        barrier(ws)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as dclk:
+            for i in range(args.steps):
+                dev_evs[i][0].record(stream)
+                dstep()
+                dev_evs[i][1].record(stream)
+            torch.cuda.synchronize()
+        barrier(ws)
+        t_dec = reduce_max(sum(a.elapsed_time(b) for a, b in dev_evs) / args.steps, ws)
+        kv_bytes = (kd.numel() + vd.numel()) * kd.element_size()
+        io_bytes = kv_bytes + qd.numel() * 2 + od.numel() * 2 + lsed.numel() * 4
+        gbps = ws * io_bytes / (t_dec * 1e-3) / 1e9
+        decode = {"workload": DECODE, "ms": round(t_dec, 4), "gbps": round(gbps, 1),
+                  "frac_of_measured_hbm": round(gbps / ws / peaks["hbm_gbs"], 4),
+                  "frac_of_8tbs_nominal": round(gbps / ws / 8000.0, 4),
+                  "algorithmic_bytes": io_bytes, "splits": nsplit, "launches_per_step": 2,
+                  "kernels": ["decode_split_kernel", "decode_merge_kernel"],
+                  "traffic": traffic_for("decode_split_kernel", ["decode.cu", "ptx.cuh", "common.cuh"]),
+                  "clocks": dclk.summary(),
+                  "l2": "inputs (2.1 GB of K/V) larger than L2; no flush"}
+        launches += args.steps * 2
+        assert sdpa.last_device_status() == 0
+
+    # ---------------------------------------------------------- CPU baseline (oracle)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = cpu_oracle_sample(w, seconds_target=15.0)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": MAIN, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "S": w.S, "E": w.E,
+                   "Ev": w.Ev, "causal": w.is_causal, "gqa": w.enable_gqa, "scale": w.scale,
+                   "step": "forward (O, LSE) + backward (dQ, dK, dV)", "seed": 0,
+                   "l2": "256 MiB flush between timed steps, outside the events",
+                   "parallelism": f"replicas x{ws} (no exchange)"},
+        "phases": phases,
+        "roofline": roof,
+        "decode": decode,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "peaks": {"source": peak_src, **peaks},
+        "gpu": props.name, "sms": sms,
+    }
+    return line
+
+
+def run_decode_only(args, ws, local, dev, peaks):
+    import torch
+
+    import scaled_dot_product_sm_gb300 as sdpa
+    import workloads
+    wd = workloads.get(DECODE)
+    qd_h, kd_h, vd_h, _, _ = workloads.make_inputs(wd, seed=0, with_grad=False)
+    qd, kd, vd = qd_h.to(dev), kd_h.to(dev), vd_h.to(dev)
+    od = torch.empty(wd.B, wd.Hq, 1, wd.Ev, dtype=qd.dtype, device=dev)
+    lsed = torch.empty(wd.B, wd.Hq, 1, dtype=torch.float32, device=dev)
+    dws = torch.empty(max(16, sdpa.decode_workspace_bytes(qd, kd, vd, 0)), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup + args.steps):
+        sdpa.sdpa_decode(qd, kd, vd, None, wd.scale, True, 0, out=od, lse=lsed, workspace=dws)
+    torch.cuda.synchronize()
+    return {"phase": "decode", "status": sdpa.last_device_status()}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_head_sample(w, nheads=1):
+    """One (batch 0) query head of the workload: inputs and nominal FLOPs of fwd+bwd on it."""
+    import torch
+
+    import workloads
+    q, k, v, dO, mask = workloads.make_inputs(w, seed=0)
+    G = w.Hq // w.Hkv
+    qs, dOs = q[:1, :nheads], dO[:1, :nheads]
+    kv_heads = sorted({h // G for h in range(nheads)})
+    ks, vs = k[:1, kv_heads], v[:1, kv_heads]
+    ms = None if mask is None else mask[:1]
+    sub = w.with_(B=1, Hq=nheads, Hkv=len(kv_heads))
+    flops = sub.flops("fwd") + sub.flops("bwd")
+    del q, k, v, dO, mask
+    return (qs, ks, vs, dOs, ms), sub, flops, torch
+
+
+def cpu_oracle_sample(w, seconds_target=15.0, steps=None):
+    import oracle
+    (qs, ks, vs, dOs, ms), sub, flops, _ = _oracle_head_sample(w)
+    times = []
+    n = 0
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv)
+        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv)
+        times.append(time.perf_counter() - t0)
+        n += 1
+        if steps is not None and n >= steps:
+            break
+        if steps is None and time.perf_counter() - t_start >= seconds_target:
+            break
+    t = statistics.median(times)
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{MAIN}: batch 0, query head 0 (1 of {w.B * w.Hq} heads), forward+backward, "
+                      f"float64 NumPy, median of {n} runs of {t:.2f} s; BLAS default threads",
+            "seconds_per_sample": round(t, 3)}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    import oracle
+    w = __import__("workloads").get(MAIN)
+    (qs, ks, vs, dOs, ms), sub, flops, _ = _oracle_head_sample(w)
+    gqa = sub.Hq != sub.Hkv
+
+    def step():
+        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, gqa)
+        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, gqa)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = (time.perf_counter() - t0) / args.steps
+    value = flops / t / 1e12
+    sample = (f"{MAIN}: batch 0, query head 0 (1 of {w.B * w.Hq} heads) per step, forward+backward, "
+              f"float64 NumPy oracle; BLAS default threads")
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": MAIN, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "S": w.S, "E": w.E,
+                       "Ev": w.Ev, "causal": w.is_causal, "gqa": w.enable_gqa, "seed": 0,
+                       "step": "forward + backward of one query head (sample)"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def summarize_launches(path):
+    """Per-kernel launches, total device time and share from an ncu --csv launch list."""
+    import collections
+    import csv
+    scale = {"ns": 1e-3, "nsecond": 1e-3, "us": 1.0, "usecond": 1.0, "ms": 1e3, "msecond": 1e3, "s": 1e6,
+             "second": 1e6}
+    rows = [r for r in csv.reader(open(path)) if r]
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    h = rows[hi]
+    ki, mi, vi, ui = (h.index(x) for x in ("Kernel Name", "Metric Name", "Metric Value", "Metric Unit"))
+    agg = collections.defaultdict(lambda: [0, 0.0])
+    for r in rows[hi + 1:]:
+        if len(r) <= vi or r[mi] != "gpu__time_duration.sum":
+            continue
+        name = r[ki].split("(")[0].replace("void ", "")
+        agg[name][0] += 1
+        agg[name][1] += float(r[vi].replace(",", "")) * scale[r[ui]]
+    tot = sum(t for _, t in agg.values())
+    lines = [f"{'kernel':78s} {'launches':>8s} {'total ms':>10s} {'share':>7s}"]
+    for k, (n, t) in sorted(agg.items(), key=lambda x: -x[1][1]):
+        lines.append(f"{k[:78]:78s} {n:8d} {t / 1e3:10.3f} {100 * t / tot:6.2f}%")
+    return "\n".join(lines)
+
+
+def main():
+    args = parse()
+    if args.summarize_launches:
+        print(summarize_launches(args.summarize_launches))
+        return
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+    else:
+        line = run_ours(args, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
