@@ -140,6 +140,39 @@ size_t sdpa_decode_workspace_bytes(const sdpa_shape* shape, int num_splits);
 /* The split count sdpa_decode uses for num_splits = 0 on the current device. */
 int sdpa_decode_num_splits(const sdpa_shape* shape);
 
+/* Size of the fixed device scratch behind sdpa_decode_noalloc: 8 MiB. */
+#define SDPA_DECODE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/* sdpa_decode without a workspace, for callers that cannot allocate device
+ * memory.  (The pages describe no such entry point: it exists for callers of
+ * this library, not for the method.)  Typical callers: an operator plugin
+ * inside another runtime that is handed its input and output tensors but no
+ * scratch, or a serving loop whose device memory is planned once at start-up
+ * and which may not call cudaMalloc afterwards (cudaMalloc can synchronise the
+ * device and fragments a fixed budget).
+ *
+ * Same arguments, result and errors as sdpa_decode, minus the workspace.  The
+ * split partials live in one file-scope device array of
+ * SDPA_DECODE_STATIC_SCRATCH_BYTES that every GPU which loads the library holds
+ * until the process exits.  A call needs B*Hq*L*num_splits*(Ev+1)*4 bytes of it
+ * (the two parts each rounded up to 256 bytes); a call that needs more returns
+ * SDPA_ERR_UNSUPPORTED before anything is enqueued.  Neither the library nor
+ * this call allocates or frees device memory.
+ *
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call uses the same array and leaves its partials
+ * there; each call overwrites all of the scratch it reads, so nothing needs
+ * clearing between calls.  Calls whose work overlaps on the GPU (other streams,
+ * other host threads) race on the array and corrupt each other's results:
+ * issue them in order on one stream. */
+sdpa_status sdpa_decode_noalloc(const sdpa_shape* shape,
+                                const void* q, const void* k, const void* v,
+                                const float* mask_or_null, double scale, int enable_gqa,
+                                int num_splits,
+                                void* o, float* lse,
+                                void* stream /* cudaStream_t */);
+
 /* Static, NUL-terminated description of a status code. */
 const char* sdpa_status_string(sdpa_status status);
 

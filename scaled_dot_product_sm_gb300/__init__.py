@@ -29,7 +29,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: 
 EXPORTS = (
     "sdpa_forward", "sdpa_forward_workspace_bytes", "sdpa_backward", "sdpa_backward_workspace_bytes",
     "sdpa_decode", "sdpa_decode_workspace_bytes", "sdpa_decode_num_splits", "sdpa_status_string",
-    "sdpa_last_device_status",
+    "sdpa_last_device_status", "sdpa_decode_noalloc",
 )
 
 
@@ -69,6 +69,9 @@ def load_library(path: Optional[str] = None):
     lib.sdpa_decode.argtypes = [SP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int, _P, _P, _P,
                                 ctypes.c_size_t, _P]
     lib.sdpa_decode.restype = ctypes.c_int
+    lib.sdpa_decode_noalloc.argtypes = [SP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int, _P, _P,
+                                        _P]
+    lib.sdpa_decode_noalloc.restype = ctypes.c_int
     for fn in ("sdpa_forward_workspace_bytes", "sdpa_backward_workspace_bytes"):
         getattr(lib, fn).argtypes = [SP]
         getattr(lib, fn).restype = ctypes.c_size_t

@@ -295,6 +295,31 @@ sdpa_status sdpa_decode(const sdpa_shape* shape, const void* q, const void* k, c
                     static_cast<cudaStream_t>(stream));
 }
 
+sdpa_status sdpa_decode_noalloc(const sdpa_shape* shape, const void* q, const void* k, const void* v,
+                                const float* mask_or_null, double scale, int enable_gqa, int num_splits, void* o,
+                                float* lse, void* stream) {
+  Checked c;
+  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
+  if (s != SDPA_OK) return s;
+  float alpha;
+  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
+  if (num_splits < 0) return SDPA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (mask_or_null && !aligned16(mask_or_null)))
+    return SDPA_ERR_INVALID_ARG;
+  if (!c.bf16 || !decode_supported(c.E, c.Ev)) return SDPA_ERR_UNSUPPORTED;
+  const int want = num_splits > 0 ? num_splits : auto_splits(c);
+  int nsplit, kps;
+  split_layout(c, want, &nsplit, &kps);
+  if (decode_ws(c, nsplit) > SDPA_DECODE_STATIC_SCRATCH_BYTES) return SDPA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  size_t cap = 0;
+  if (decode_static_scratch(&scratch, &cap) != cudaSuccess) return SDPA_ERR_CUDA;
+  return run_decode(c, q, k, v, mask_or_null, alpha, want, o, lse, scratch, cap,
+                    static_cast<cudaStream_t>(stream));
+}
+
 size_t sdpa_decode_workspace_bytes(const sdpa_shape* shape, int num_splits) {
   Checked c;
   if (check_shape(shape, 1, false, &c) != SDPA_OK || num_splits < 0) return 0;

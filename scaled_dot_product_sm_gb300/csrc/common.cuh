@@ -95,6 +95,9 @@ bool bwd_tc_supported(int E, int Ev);
 bool decode_supported(int E, int Ev);
 int decode_rows_per_cta();
 int decode_stage_keys();
+// Device address and size of the fixed decode scratch on the current device
+// (looked up on first use per device).
+cudaError_t decode_static_scratch(void** ptr, size_t* bytes);
 
 // Tensor-map encoder obtained from the driver at run time (no libcuda link).
 bool encode_tmap_bf16_3d(void* tmap /* CUtensorMap* */, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,

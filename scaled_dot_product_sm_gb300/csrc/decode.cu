@@ -20,8 +20,11 @@
 // contributing nothing and an all-empty row giving o = 0, lse = -inf.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
+#include "sdpa.h"
 
 namespace sdpa_impl {
 
@@ -351,6 +354,38 @@ cudaError_t launch_decode(const DecodeParams& dp, cudaStream_t st) {
   if (ech == 1 && vch == 1) return run<1, 1>(dp, st);
   if (ech == 2 && vch == 1) return run<2, 1>(dp, st);
   return run<1, 2>(dp, st);
+}
+
+// ---------------------------------------------------------------- fixed scratch
+// Split partials of sdpa_decode_noalloc, for callers that cannot hand the
+// library a workspace.  A file-scope device array: every GPU that loads the
+// library holds one copy of SDPA_DECODE_STATIC_SCRATCH_BYTES until the process
+// exits.  Host code must not pass g_decode_scratch itself to a kernel (on the
+// host that name is only a stand-in); decode_static_scratch() looks up its
+// device address once per device, with that device current.
+static __device__ __align__(256) unsigned char g_decode_scratch[SDPA_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kScratchDevices] = {};
+}  // namespace
+
+cudaError_t decode_static_scratch(void** ptr, size_t* bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = addr;
+  }
+  *ptr = g_scratch_addr[dev];
+  *bytes = sizeof(g_decode_scratch);
+  return cudaSuccess;
 }
 
 }  // namespace sdpa_impl
