@@ -170,10 +170,21 @@ bool routes_to_decode(const Checked& c, bool has_mask, int causal) {
   return c.bf16 && c.L == 1 && !causal && decode_supported(c.E, c.Ev);
 }
 
+bool bwd_uses_tc(const Checked& c) { return c.bf16 && bwd_tc_supported(c.E, c.Ev); }
+
+// Tensor-core backward: per-row (-lse*log2e, D) float2 rows padded per head to a
+// multiple of the query tile, then the fp32 dQ accumulator.  CUDA-core backward:
+// D only.
+size_t bwd_stats_bytes(const Checked& c) {
+  if (!bwd_uses_tc(c)) return round_up(static_cast<size_t>(c.B) * c.Hq * c.L * sizeof(float), 256);
+  const size_t pad = static_cast<size_t>(bwd_tc_row_pad());
+  const size_t lpad = (static_cast<size_t>(c.L) + pad - 1) / pad * pad;
+  return round_up(static_cast<size_t>(c.B) * c.Hq * lpad * 2 * sizeof(float), 256);
+}
+
 size_t bwd_ws(const Checked& c) {
-  const size_t rows = static_cast<size_t>(c.B) * c.Hq * c.L;
-  size_t bytes = round_up(rows * sizeof(float), 256);
-  if (c.bf16 && bwd_tc_supported(c.E, c.Ev)) bytes += round_up(rows * c.E * sizeof(float), 256);
+  size_t bytes = bwd_stats_bytes(c);
+  if (bwd_uses_tc(c)) bytes += round_up(static_cast<size_t>(c.B) * c.Hq * c.L * c.E * sizeof(float), 256);
   return bytes;
 }
 
@@ -359,11 +370,9 @@ sdpa_status sdpa_backward(const sdpa_shape* shape, const void* q, const void* k,
   p.dO = dO;
   p.lse = lse;
   p.mask = mask_or_null;
-  const size_t rows = static_cast<size_t>(c.B) * c.Hq * c.L;
   p.D = static_cast<float*>(workspace);
-  p.dq_acc = (c.bf16 && bwd_tc_supported(c.E, c.Ev))
-                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * sizeof(float), 256))
-                 : nullptr;
+  p.dq_acc = bwd_uses_tc(c) ? reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_stats_bytes(c))
+                            : nullptr;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -382,9 +391,12 @@ sdpa_status sdpa_backward(const sdpa_shape* shape, const void* q, const void* k,
   p.causal = is_causal ? 1 : 0;
   p.status = status_ptr();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.dq_acc) {
+    if (c.B * c.Hkv > 65535 * 64 || (c.S + 127) / 128 > 65535) return SDPA_ERR_UNSUPPORTED;
+    return from_cuda(launch_bwd_tc(p, st));
+  }
   cudaError_t e = launch_bwd_preprocess(p, c.bf16 ? 1 : 0, st);
   if (e != cudaSuccess) return SDPA_ERR_CUDA;
-  if (p.dq_acc) return from_cuda(launch_bwd_tc(p, st));
   if ((c.L + 15) / 16 > 65535 || (c.S + 15) / 16 > 65535 || static_cast<long long>(c.B) * c.Hq > 65535)
     return SDPA_ERR_UNSUPPORTED;
   return from_cuda(launch_bwd_simt(p, c.bf16 ? 1 : 0, st));

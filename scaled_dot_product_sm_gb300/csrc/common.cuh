@@ -92,6 +92,7 @@ cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
 bool fwd_tc_supported(int E, int Ev);
 bool bwd_tc_supported(int E, int Ev);
+int bwd_tc_row_pad();   // query rows of the tensor-core backward's row-statistics padding
 bool decode_supported(int E, int Ev);
 int decode_rows_per_cta();
 int decode_stage_keys();

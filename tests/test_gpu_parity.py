@@ -159,6 +159,9 @@ BF16_CASES = [
     (1, 2, 1, 256, 256, 128, 64, True, "block", (1, 1), 1),
     (1, 2, 2, 129, 129, 64, 128, False, "none", None, 0),
     (1, 2, 2, 96, 80, 32, 40, True, "bias", (1, 1), 1),     # widths outside {64,128}: CUDA-core path
+    (1, 8, 2, 100, 300, 128, 128, True, "none", None, 0),   # key tiles past every query: dK = dV = 0
+    (2, 4, 1, 333, 333, 128, 128, True, "bias", (2, 4), 2), # GQA causal + per-head mask, ragged
+    (1, 2, 2, 64, 1000, 128, 128, False, "block", (1, 2), 0),
 ]
 
 

@@ -1,0 +1,102 @@
+"""Full-size workloads, in the launch configuration the benchmark times.
+
+Each workload runs whole on the GPU; the float64 oracle then recomputes
+sampled closed sub-problems (whole KV groups: the Hq/Hkv query heads sharing a
+KV head, with all their keys and queries) and every output of those groups is
+compared with the same tolerances as the small cases.  Properties that hold at
+any size are checked on the whole tensors: no NaN/Inf, LSE = -inf exactly on
+fully masked rows (and only there), zero O/dQ rows there, and zero dK/dV rows
+for keys that no query may see.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_dot_product_sm_gb300 as sdpa
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+BF_O, BF_G, BF_LSE = 5e-3, 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sdpa.build()
+    sdpa.load_library()
+
+
+def rel_l2(x, ref):
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def run_workload(name, groups):
+    w = workloads.get(name)
+    q, k, v, dO, mask = workloads.make_inputs(w, seed=0, with_grad="bwd" in w.phases)
+    dev = [None if x is None else x.cuda() for x in (q, k, v, dO, mask)]
+    qd, kd, vd, dOd, md = dev
+    o, lse = sdpa.sdpa_forward(qd, kd, vd, md, w.scale, w.is_causal, w.enable_gqa)
+    grads = None
+    if "bwd" in w.phases:
+        grads = sdpa.sdpa_backward(qd, kd, vd, o, dOd, lse, md, w.scale, w.is_causal, w.enable_gqa)
+    torch.cuda.synchronize()
+    assert sdpa.last_device_status() == 0
+    assert torch.isfinite(o).all()
+    if grads is not None:
+        for g in grads:
+            assert torch.isfinite(g).all()
+    G = w.Hq // w.Hkv
+    for b, kv in groups:
+        sl = slice(kv * G, (kv + 1) * G)
+        out = oracle.ref_group(q, k, v, dO, b, kv, mask, w.scale, w.is_causal)
+        ref_o, ref_lse = out[0], out[1]
+        lg = lse[b, sl].double().cpu().numpy()
+        dead = np.isneginf(ref_lse)
+        assert np.array_equal(np.isneginf(lg), dead)
+        assert np.abs(lg[~dead] - ref_lse[~dead]).max() <= BF_LSE
+        og = f64(o[b, sl])
+        assert np.all(og[dead] == 0.0)
+        assert rel_l2(og, ref_o) <= BF_O, (name, b, kv, rel_l2(og, ref_o))
+        if grads is not None:
+            dq, dk, dv = grads
+            e_q = rel_l2(f64(dq[b, sl]), out[2])
+            e_k = rel_l2(f64(dk[b, kv]), out[3])
+            e_v = rel_l2(f64(dv[b, kv]), out[4])
+            assert max(e_q, e_k, e_v) <= BF_G, (name, b, kv, e_q, e_k, e_v)
+            assert np.all(f64(dq[b, sl])[dead] == 0.0)
+    return w, q, k, v, mask, o, lse, grads
+
+
+def test_mha_causal_e64():
+    run_workload("mha_causal_e64", [(0, 0), (3, 15)])
+
+
+def test_gqa_causal_e128():
+    run_workload("gqa_causal_e128", [(0, 0), (1, 7)])
+
+
+def test_padded_mask_e128():
+    w, q, k, v, mask, o, lse, grads = run_workload("padded_mask_e128", [(0, 0), (5, 9)])
+    m = mask[:, 0]                                         # [B, L, S]
+    dead_rows = torch.isneginf(m).all(dim=-1)              # [B, L]
+    lse_dead = torch.isneginf(lse).cpu()                   # [B, H, L]
+    assert torch.equal(lse_dead, dead_rows[:, None, :].expand_as(lse_dead))
+    assert (o.cpu()[dead_rows[:, None, :].expand(-1, w.Hq, -1)] == 0).all()
+    dq, dk, dv = grads
+    assert (dq.cpu()[dead_rows[:, None, :].expand(-1, w.Hq, -1)] == 0).all()
+    dead_keys = torch.isneginf(m).all(dim=1)               # [B, S]: blocked for every query
+    sel = dead_keys[:, None, :].expand(-1, w.Hkv, -1)
+    assert (dk.cpu()[sel] == 0).all() and (dv.cpu()[sel] == 0).all()
+
+
+def test_gqa_decode_s32k():
+    run_workload("gqa_decode_s32k", [(0, 0), (15, 7)])
