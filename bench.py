@@ -54,8 +54,8 @@ def parse():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--phase", choices=["all", "fwd", "decode"], default="all",
-                    help="profiling aid: run only the forward loop or only the decode leg")
+    ap.add_argument("--phase", choices=["all", "fwd", "bwd", "decode"], default="all",
+                    help="profiling aid: run only the forward loop, the backward loop or the decode leg")
     ap.add_argument("--summarize-launches", metavar="CSV",
                     help="print a per-kernel summary of an ncu launch list (gpu__time_duration.sum, --csv) and exit")
     args = ap.parse_args()
@@ -227,6 +227,12 @@ def run_ours(args, ws, rank, local):
     if args.phase == "decode":
         return run_decode_only(args, ws, local, dev, peaks)
     fwd_only = args.phase == "fwd"
+    if args.phase == "bwd":
+        fwd()
+        for _ in range(args.warmup + args.steps):
+            bwd()
+        torch.cuda.synchronize()
+        return {"phase": "bwd", "status": sdpa.last_device_status()}
     for _ in range(args.warmup):
         fwd()
         if not fwd_only:

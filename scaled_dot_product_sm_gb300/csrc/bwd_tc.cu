@@ -14,7 +14,7 @@
 //     and the fp32 dQ accumulator zeroed;
 //  2. the main kernel, one CTA per (batch, KV head, 128-key tile).  K and V stay
 //     in shared memory; the CTA walks the Hq/Hkv query heads of its group and
-//     their 64-row query tiles (from the diagonal on when causal), so dK and dV
+//     their 64-row query tiles (last to first, down to the diagonal when causal), so dK and dV
 //     are summed over the group inside the CTA (no atomics for them):
 //        S^T  = K Q^T          (TMEM, 128 keys x 64 queries)
 //        dP^T = V dO^T         (TMEM)
@@ -48,7 +48,7 @@ constexpr int E = 128, Ev = 128;
 constexpr int BKV = 128;       // keys per CTA
 constexpr int BQ = 64;         // queries per iteration
 constexpr int kThreads = 320;
-constexpr int kNSQ = 2;        // query-tile stages
+constexpr int kNSQ = 3;        // query-tile stages (prefetch two tiles ahead)
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // shared memory map (bytes; every operand block 1024-aligned)
@@ -156,6 +156,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt_begin = p.causal ? min(k0 / BQ, nqt) : 0;
   const int per_head = nqt - qt_begin;
   const int n = p.G * per_head;                          // iterations
+  // Iteration i -> (query tile, head): tiles from the last down to the diagonal,
+  // the group's heads innermost.  Every CTA of a KV group starts at the same
+  // (last) tile and walks down in step, so the CTAs running at the same time
+  // read the same Q/dO tiles and mostly hit in L2.
+  auto tile_of = [&](int i, int& qt, int& g) {
+    qt = nqt - 1 - i / p.G;
+    g = i - (i / p.G) * p.G;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -164,13 +172,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
+    mbar_init(s_free, 4);     // one arrival per elementwise warp
     mbar_init(dp_full, 1);
-    mbar_init(dp_free, 128);
-    mbar_init(p_full, 128);
+    mbar_init(dp_free, 4);
+    mbar_init(p_full, 4);
     mbar_init(p_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, 4);    // one arrival per drain warp
     mbar_init(kdv_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -198,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < n; ++i) {
         const int s = i % kNSQ;
-        const int g = i / per_head, qt = qt_begin + (i - g * per_head);
+        int qt, g;
+        tile_of(i, qt, g);
         const int bh = b * p.Hq + hkv * p.G + g;
         mbar_wait(&q_empty[s], ((i / kNSQ) & 1) ^ 1, abort_flag, p.status, status_code(0x31));
         uint8_t* st = smem + kOffStage + s * kStage;
@@ -284,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* dsrow = smem + kOffDS + r * 128;
     for (int i = 0; i < n; ++i) {
       const int s = i % kNSQ;
-      const int g = i / per_head, qt = qt_begin + (i - g * per_head);
+      int qt, g;
+      tile_of(i, qt, g);
       const int h = hkv * p.G + g;
       const int q0 = qt * BQ;
       const float2* rs = reinterpret_cast<const float2*>(smem + kOffStage + s * kStage + 2 * kQTile);
@@ -302,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(v[j]);
       }
       tc_fence_before();
-      mbar_arrive(s_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
       const float* mcol = (p.mask && key < p.S)
                               ? p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(q0) * p.S + key
                               : nullptr;
@@ -328,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j) d[32 + j] = __uint_as_float(v[j]);
       }
       tc_fence_before();
-      mbar_arrive(dp_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dp_free);
 #pragma unroll
       for (int j = 0; j < BQ; ++j) d[j] = x[j] * (d[j] - rs[j].y);   // dS^T
       if (i > 0) mbar_wait(p_free, (i - 1) & 1, abort_flag, p.status, status_code(0x3b));
@@ -349,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
     }
     // ---------------------------------------------------------- dK, dV epilogue
     __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bkv) * p.S + key) * E;
@@ -390,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = (warp - 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     for (int i = 0; i < n; ++i) {
-      const int g = i / per_head, qt = qt_begin + (i - g * per_head);
+      int qt, g;
+      tile_of(i, qt, g);
       const int bh = b * p.Hq + hkv * p.G + g;
       const int q0 = qt * BQ;
       mbar_wait(dq_full, i & 1, abort_flag, p.status, status_code(0x3d));
@@ -399,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + kColDQ, v0);
       tmem_ld32(tmem + lane_off + kColDQ + 32, v1);
       tc_fence_before();
-      mbar_arrive(dq_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
       float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.L + q0) * E + e;
       const int nq = min(BQ, p.L - q0);
 #pragma unroll

@@ -9,17 +9,19 @@
 // that share every K/V tile load.  Warp roles (320 threads):
 //   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax of query tile 1
-//   warp  8    TMA producer: Q tiles once, then K_j, V_j through an NS-stage ring
+//   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through a ring
 //   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+Ev), O_1 [384,384+Ev).
-// The MMA issue order per key tile j is  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1),
-// so the tensor core works on one query tile while the other tile's softmax
-// runs.  A commit after S_t(j+1) also covers PV_t(j), so when the softmax of
-// tile t sees S_t(j+1) ready, O_t is complete and its P buffer is free.
-// P goes to shared memory as bf16 in the 128-byte-swizzled K-major layout the
-// MMA reads.  Exponentials are exp2 with alpha*log2(e) folded into the scale;
-// O is only rescaled when a row's max grows by more than 2^8 (the stale max
-// keeps every p below 256, and O/l is exact either way).
+// The softmax writes P_t as bf16 pairs over the first 64 columns of S_t, and
+// O_t += P_t V reads it straight from TMEM (A operand in TMEM), so P never
+// touches shared memory and the tensor core reads only K, V and Q from it.
+// MMA issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): the
+// tensor core works on one query tile while the other tile's softmax runs, and
+// S_t(j+1) (which overwrites P_t(j)'s columns) follows PV_t(j) in the same
+// in-order MMA stream.  The commit after S_t(j+1) also covers PV_t(j), so when
+// tile t sees its next scores, O_t is complete.  Exponentials are exp2 with alpha*log2(e)
+// folded into the scale; O is only rescaled when a row's max grows by more
+// than 2^8 (the stale max keeps every p below 256, and O/l is exact either way).
 // Causal: key tiles entirely above the diagonal are neither loaded nor
 // computed; only tiles that cross it test j <= i per element.
 #include <cuda.h>
@@ -51,16 +53,14 @@ struct FwdCfg {
   static constexpr int E = ECH * 64, Ev = VCH * 64;
   static constexpr int kQBytes = ECH * kChunkBytes;                          // one query tile
   static constexpr int kItem = (ECH > VCH ? ECH : VCH) * kChunkBytes;       // one K or V tile
-  static constexpr int kPBytes = 2 * kChunkBytes;                            // 128 x 128 bf16
-  static constexpr int kFixed = 2 * kQBytes + 2 * kPBytes;
+  static constexpr int kFixed = 2 * kQBytes;
   static constexpr int kBudget = 227 * 1024 - 2048;
   static constexpr int NS = (kBudget - kFixed) / kItem > 8 ? 8 : (kBudget - kFixed) / kItem;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;
-  static constexpr int kOffRing = kOffP + 2 * kPBytes;
+  static constexpr int kOffRing = kOffQ + 2 * kQBytes;
   static constexpr int kOffBar = kOffRing + NS * kItem;
   static constexpr int kBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
-  static_assert(NS >= 2, "not enough shared memory for a 2-stage ring");
+  static_assert(NS >= 2, "the K/V ring needs two stages");
 };
 
 template <int ECH, int VCH>
@@ -75,9 +75,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_q = bar;                 // 1
   uint64_t* full = bar + 1;              // NS
   uint64_t* empty = full + NS;           // NS
-  uint64_t* s_full = empty + NS;         // 2
-  uint64_t* p_full = s_full + 2;         // 2
-  uint64_t* o_final = p_full + 2;        // 2
+  uint64_t* s_full = empty + NS;         // 2: S_t(j) (and PV_t(j-1)) complete
+  uint64_t* p_full = s_full + 2;         // 2: P_t(j) in TMEM (one arrival per warp)
+  uint64_t* o_final = p_full + 2;        // 2: the last PV_t complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       n_t[t] = (kmax + BN - 1) / BN;
     }
   }
-  const int n = max(n_t[0], n_t[1]);
+  const int n = max(n_t[0], n_t[1]);   // n_t[0] <= n_t[1] unless tile 1 is past L
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], BM);
+      mbar_init(&p_full[t], 4);
       mbar_init(&o_final[t], 1);
     }
     *abort_flag = 0;
@@ -135,26 +135,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < ECH; ++c)
           tma_load_3d(smem + C::kOffQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar_q, c * 64, r0 + t * BM, bh);
       }
+      // ring order = consumption order: K_0, then per j: V_j, K_{j+1} (if any)
       int it = 0;
+      auto load = [&](bool is_k, int j) {
+        const int s = it % NS;
+        mbar_wait(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.status, status_code(0x11));
+        uint8_t* dst = smem + C::kOffRing + s * C::kItem;
+        const int ch = is_k ? ECH : VCH;
+        mbar_arrive_expect_tx(&full[s], ch * kChunkBytes);
+        for (int c = 0; c < ch; ++c)
+          tma_load_3d(dst + c * kChunkBytes, is_k ? &tmK : &tmV, &full[s], c * 64, j * BN, bkv);
+        ++it;
+      };
+      load(true, 0);
       for (int j = 0; j < n; ++j) {
-        for (int kv = 0; kv < 2; ++kv, ++it) {
-          const int s = it % NS;
-          mbar_wait(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.status, status_code(0x11));
-          uint8_t* dst = smem + C::kOffRing + s * C::kItem;
-          const int ch = kv == 0 ? ECH : VCH;
-          mbar_arrive_expect_tx(&full[s], ch * kChunkBytes);
-          for (int c = 0; c < ch; ++c)
-            tma_load_3d(dst + c * kChunkBytes, kv == 0 ? &tmK : &tmV, &full[s], c * 64, j * BN, bkv);
-        }
+        load(false, j);
+        if (j + 1 < n) load(true, j + 1);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);        // Q (K-major) x K (K-major)
-      constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (K-major) x V (MN-major)
+      constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (TMEM, K-major) x V (MN-major)
       const uint32_t q_addr = smem_u32(smem + C::kOffQ);
-      const uint32_t p_addr = smem_u32(smem + C::kOffP);
       const uint32_t ring = smem_u32(smem + C::kOffRing);
       auto issue_s = [&](int t, uint32_t kaddr) {
         const uint32_t qa = q_addr + t * C::kQBytes;
@@ -166,17 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
-        const uint32_t pa = p_addr + t * C::kPBytes;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          umma_ss(tmem + 256 + t * 128, sdesc_sw128(pa + aoff, 16, 1024),
+        for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 8 TMEM columns of bf16 pairs per step
+          umma_ts(tmem + 256 + t * 128, tmem + t * BN + kk * 8,
                   sdesc_sw128(vaddr + kk * 16 * 128, kChunkBytes, 1024), idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
       };
       mbar_wait(bar_q, 0, abort_flag, p.status, status_code(0x12));
       int it = 0;
-      // S_t(0)
       {
         const int s = it % NS;
         mbar_wait(&full[s], (it / NS) & 1, abort_flag, p.status, status_code(0x13));
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               ++it;
             }
-            issue_s(t, ring + sk * C::kItem);
+            issue_s(t, ring + sk * C::kItem);   // overwrites P_t(j) after PV_t(j) in issue order
             umma_commit(&s_full[t]);
           } else {
             umma_commit(&o_final[t]);
@@ -228,22 +228,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
       const uint32_t tS = tmem + lane_off + t * BN;
       const uint32_t tO = tmem + lane_off + 256 + t * 128;
-      uint8_t* prow = smem + C::kOffP + t * C::kPBytes + r * 128;
       const float* mrow = (p.mask && row < p.L)
                               ? p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(row) * p.S
                               : nullptr;
       const int row_first = r0 + t * BM;   // first row of this tile
+      const float sc = p.scale_log2;
       float m_run = kNegInf, l_run = 0.f;
       for (int j = 0; j < nt; ++j) {
-        mbar_wait(&s_full[t], j & 1, abort_flag, p.status, status_code(0x17));
+        mbar_wait(&s_full[t], j & 1, abort_flag, p.status, status_code(0x18));
         tc_fence_after();
         float x[BN];
+        {
+          uint32_t v[BN];
+          tmem_ld128(tS, v);
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + c * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(v[i]) * p.scale_log2;
+          for (int i = 0; i < BN; i += 2)
+            mul2(x[i], x[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sc, sc);
         }
         const int kb = j * BN;
         if (mrow) {
@@ -254,10 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int key = kb + 4 * c;
               if (key < p.S) {
                 const float4 mv = __ldg(reinterpret_cast<const float4*>(mrow + key));
-                x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
-                x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
-                x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
-                x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
+                fma2(x[4 * c + 0], x[4 * c + 1], mv.x, mv.y, kLog2e, kLog2e, x[4 * c + 0], x[4 * c + 1]);
+                fma2(x[4 * c + 2], x[4 * c + 3], mv.z, mv.w, kLog2e, kLog2e, x[4 * c + 2], x[4 * c + 3]);
               }
             }
           } else {
@@ -276,51 +274,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BN; ++i)
             if (kb + i > row) x[i] = kNegInf;
         }
-        float mx = x[0];
+        // row max: eight independent chains of three-input maxima
+        float mx8[8];
 #pragma unroll
-        for (int i = 1; i < BN; ++i) mx = fmaxf(mx, x[i]);
+        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(x[u], x[8 + u]);
+#pragma unroll
+        for (int i = 16; i < BN; i += 16)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx8[u] = max3f(mx8[u], x[i + u], x[i + 8 + u]);
+        const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
         const float m_new = fmaxf(m_run, mx);
         const bool need = m_new > m_run + kRescaleThreshold;
         const float m_use = need ? m_new : m_run;
-        const float msafe = (m_use == kNegInf) ? 0.f : m_use;
-        const float corr = need ? ex2(m_run - msafe) : 1.f;
-        // p = exp2(x - m), row sum, bf16 P into the swizzled smem tile
-        float rs = 0.f;
+        const float nm = (m_use == kNegInf) ? 0.f : -m_use;
+        const float corr = need ? ex2(m_run + nm) : 1.f;
+        // p = exp2(x - m), packed to bf16 pairs; row sum in eight independent chains
+        uint32_t pk[BN / 2];
+        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < BN / 8; ++c) {
-          float pv[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            pv[u] = ex2(x[c * 8 + u] - msafe);
-            rs += pv[u];
-          }
-          uint4 w;
-          w.x = pack_bf16x2(pv[0], pv[1]);
-          w.y = pack_bf16x2(pv[2], pv[3]);
-          w.z = pack_bf16x2(pv[4], pv[5]);
-          w.w = pack_bf16x2(pv[6], pv[7]);
-          const int chunk = c & 7, half = c >> 3;
-          *reinterpret_cast<uint4*>(prow + half * kChunkBytes + ((chunk ^ (r & 7)) << 4)) = w;
+        for (int i = 0; i < BN; i += 2) {
+          float a0, a1;
+          add2(a0, a1, x[i], x[i + 1], nm, nm);
+          a0 = ex2(a0);
+          a1 = ex2(a1);
+          const int u = (i >> 1) & 3;
+          add2(rs8[2 * u], rs8[2 * u + 1], rs8[2 * u], rs8[2 * u + 1], a0, a1);
+          pk[i >> 1] = pack_bf16x2(a0, a1);
         }
+        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l_run = l_run * corr + rs;
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (j > 0) {
+          // O_t holds PV_t(0..j-1) (complete: the commit after S_t(j) covered it)
+          if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int c = 0; c < C::Ev / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tO + c * 32, v);
+            for (int c = 0; c < C::Ev / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tO + c * 32, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-            tmem_st32(tO + c * 32, v);
+              for (int i = 0; i < 32; i += 2) {
+                float y0, y1;
+                mul2(y0, y1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), corr, corr);
+                v[i] = __float_as_uint(y0);
+                v[i + 1] = __float_as_uint(y1);
+              }
+              tmem_st32(tO + c * 32, v);
+            }
           }
-          tmem_wait_st();
         }
         m_run = m_use;
-        fence_proxy_async_smem();
+        {
+          // P_t(j) over the first 64 columns of S_t: column c holds keys 2c (low) and 2c+1 (high)
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) w[c] = pk[c];
+          tmem_st32(tS, w);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) w[c] = pk[32 + c];
+          tmem_st32(tS + 32, w);
+        }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[t]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
       }
       // ---------------------------------------------------------- epilogue
-      mbar_wait(&o_final[t], 0, abort_flag, p.status, status_code(0x18));
+      mbar_wait(&o_final[t], 0, abort_flag, p.status, status_code(0x1a));
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.L + row) * C::Ev;
