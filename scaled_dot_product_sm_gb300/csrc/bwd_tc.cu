@@ -14,23 +14,27 @@
 //     and the fp32 dQ accumulator zeroed;
 //  2. the main kernel, one CTA per (batch, KV head, 128-key tile).  K and V stay
 //     in shared memory; the CTA walks the Hq/Hkv query heads of its group and
-//     their 64-row query tiles (last to first, down to the diagonal when causal), so dK and dV
-//     are summed over the group inside the CTA (no atomics for them):
-//        S^T  = K Q^T          (TMEM, 128 keys x 64 queries)
-//        dP^T = V dO^T         (TMEM)
+//     their 64-row query tiles (last to first, down to the diagonal when
+//     causal), so dK and dV are summed over the group inside the CTA:
+//        S^T  = K Q^T                       (TMEM, 128 keys x 64 queries)
+//        dP^T = V dO^T                      (TMEM)
 //        P^T  = exp2(S^T alpha log2e + mask log2e - lse log2e),  dS^T = P^T o (dP^T - D)
-//        dV  += P^T dO,  dK += dS^T Q     (TMEM accumulators, 128 x 128 each)
-//        dQ^T = K^T dS^T       (TMEM, 128 head dims x 64 queries)
-//     dQ^T puts the head dimension on the TMEM lanes, so the four drain warps
-//     add each query's 128 fp32 values to the global accumulator with fully
-//     coalesced reductions (red.global.add.f32, 128 bytes per warp instruction);
+//        dV  += P^T dO,  dK += dS^T Q       (A operands P^T, dS^T read from TMEM)
+//        dQ^T = K^T dS^T                    (TMEM, 128 head dims x 64 queries; dS^T also in smem)
+//     dQ^T is staged in shared memory as dQ rows and added to the global fp32
+//     accumulator with one TMA bulk reduction per tile (the reduction runs in
+//     L2, full lines, one instruction);
 //  3. dQ = bf16(accumulator).
-// Warp roles (320 threads): warps 0-3 elementwise (thread = key = TMEM lane),
-// warps 4-7 dQ drain (thread = head dim = TMEM lane), warp 8 TMA producer,
-// warp 9 TMEM allocator and single-thread MMA issuer.  S^T(i+1) and dP^T(i+1)
-// are issued as soon as the elementwise warps have read S^T(i) and dP^T(i), so
-// the tensor core computes the next scores while the current gradients wait for
-// P^T and dS^T.
+// Warp roles (384 threads, three warpgroups with a register split):
+//   warps 0-3   elementwise (thread = key = TMEM lane)                 232 regs
+//   warps 4-7   dQ drain and staging (thread = head dim = TMEM lane)    216 regs
+//   warp  8     TMA producer, warp 9 TMEM allocator and MMA issuer,      56 regs
+//   warps 10-11 idle (they complete the third warpgroup)
+// TMEM (512 columns): dK [0,128), dV [128,256), S^T [256,320), dP^T [320,384),
+// dQ^T [384,448), P^T bf16 [448,480), dS^T bf16 [480,512).
+// S^T(i+1) and dP^T(i+1) are issued as soon as the elementwise warps have read
+// S^T(i) and dP^T(i), so the tensor core computes the next scores while the
+// current gradients wait for P^T and dS^T.
 #include <cuda.h>
 
 #include <algorithm>
@@ -47,9 +51,14 @@ using namespace sdpa_ptx;
 constexpr int E = 128, Ev = 128;
 constexpr int BKV = 128;       // keys per CTA
 constexpr int BQ = 64;         // queries per iteration
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kNSQ = 3;        // query-tile stages (prefetch two tiles ahead)
 constexpr float kNegInf = -__builtin_huge_valf();
+
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsElem = 232, kRegsDrain = 216, kRegsOther = 56;
+static_assert(128 * (kRegsElem + kRegsDrain + kRegsOther) <= kThreads * kRegsLaunch, "register split too large");
+static_assert(kRegsElem + kRegsDrain + kRegsOther <= 512, "per sub-partition register file exceeded");
 
 // shared memory map (bytes; every operand block 1024-aligned)
 constexpr int kKBytes = 2 * BKV * 128;                 // K tile: 2 chunks of [128 keys x 64 dims]
@@ -58,13 +67,13 @@ constexpr int kStage = 2 * kQTile + 1024;              // Q, dO, rowstats (512 B
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKBytes;
 constexpr int kOffStage = kOffV + kKBytes;
-constexpr int kOffP = kOffStage + kNSQ * kStage;       // P^T [128 keys x 64 queries] bf16
-constexpr int kOffDS = kOffP + BKV * 128;              // dS^T
-constexpr int kOffBar = kOffDS + BKV * 128;
+constexpr int kOffDS = kOffStage + kNSQ * kStage;      // dS^T [128 keys x 64 queries] bf16 (B operand of dQ^T)
+constexpr int kOffDQ = kOffDS + BKV * 128;             // dQ staging [64 queries x 128 dims] fp32
+constexpr int kOffBar = kOffDQ + BQ * E * 4;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
 
 // TMEM columns
-constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 320, kColDQ = 384;
+constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 320, kColDQ = 384, kColP = 448, kColDS = 480;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -72,9 +81,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 struct TcBwdArgs {
   BwdParams p;
@@ -192,9 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n > 0) {
+  if (warp >= 8) {
+    regs_dec<kRegsOther>();
+    if (warp == 8 && lane == 0 && n > 0) {
+      // ---------------------------------------------------------- TMA producer
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmQ);
@@ -218,15 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bulk_load(st + 2 * kQTile, a.rowstats + static_cast<size_t>(bh) * a.Lpad + qt * BQ, BQ * 8, &q_full[s]);
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    } else if (warp == 9 && lane == 0 && n > 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T: K-major x K-major
-      constexpr uint32_t id_kv = idesc_bf16(BKV, E, 0, 1);     // dV, dK: K-major x MN-major
+      constexpr uint32_t id_kv = idesc_bf16(BKV, E, 0, 1);     // dV, dK: TMEM (K-major) x MN-major
       constexpr uint32_t id_q = idesc_bf16(E, BQ, 1, 1);       // dQ^T: MN-major x MN-major
       const uint32_t kA = smem_u32(smem + kOffK), vA = smem_u32(smem + kOffV);
-      const uint32_t pA = smem_u32(smem + kOffP), dsA = smem_u32(smem + kOffDS);
+      const uint32_t dsA = smem_u32(smem + kOffDS);
       const uint32_t stage0 = smem_u32(smem + kOffStage);
       mbar_wait(kv_full, 0, abort_flag, p.status, status_code(0x32));
       auto issue_sdp = [&](int i) {
@@ -263,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(p_full, i & 1, abort_flag, p.status, status_code(0x36));
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {   // dV += P^T dO ; dK += dS^T Q   (K = queries)
-          umma_ss(tmem + kColDV, sdesc_sw128(pA + kk * 32, 16, 1024),
-                  sdesc_sw128(doA + kk * 16 * 128, BQ * 128, 1024), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          umma_ss(tmem + kColDK, sdesc_sw128(dsA + kk * 32, 16, 1024),
-                  sdesc_sw128(qA + kk * 16 * 128, BQ * 128, 1024), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BQ / 16; ++kk) {   // dV += P^T dO ; dK += dS^T Q   (K = queries; 16 = 8 cols)
+          umma_ts(tmem + kColDV, tmem + kColP + kk * 8, sdesc_sw128(doA + kk * 16 * 128, BQ * 128, 1024), id_kv,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + kColDK, tmem + kColDS + kk * 8, sdesc_sw128(qA + kk * 16 * 128, BQ * 128, 1024), id_kv,
+                  (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&q_empty[s]);
         if (i > 0) {
@@ -285,19 +301,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(kdv_done);
     }
   } else if (warp < 4) {
+    regs_inc<kRegsElem>();
     // ------------------------------------------------------------ elementwise warps (thread = key)
     const int r = warp * 32 + lane;
     const int key = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    uint8_t* prow = smem + kOffP + r * 128;
     uint8_t* dsrow = smem + kOffDS + r * 128;
+    const float sc = p.scale_log2;
     for (int i = 0; i < n; ++i) {
       const int s = i % kNSQ;
       int qt, g;
       tile_of(i, qt, g);
       const int h = hkv * p.G + g;
       const int q0 = qt * BQ;
-      const float2* rs = reinterpret_cast<const float2*>(smem + kOffStage + s * kStage + 2 * kQTile);
+      const float4* rs4 = reinterpret_cast<const float4*>(smem + kOffStage + s * kStage + 2 * kQTile);
       mbar_wait(&q_full[s], (i / kNSQ) & 1, abort_flag, p.status, status_code(0x38));
       mbar_wait(s_full, i & 1, abort_flag, p.status, status_code(0x39));
       tc_fence_after();
@@ -314,18 +331,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
-      const float* mcol = (p.mask && key < p.S)
-                              ? p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(q0) * p.S + key
-                              : nullptr;
-      const bool dead_key = key >= p.S;
-      const bool diag = p.causal && (k0 + BKV - 1 > q0);
+      // t = s alpha log2e - lse log2e  (rowstats hold (-lse log2e, D) per query: two queries per float4)
 #pragma unroll
-      for (int j = 0; j < BQ; ++j) {
-        float t = fmaf(x[j], p.scale_log2, rs[j].x);
-        if (mcol && q0 + j < p.L) t = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, t);
-        if (dead_key || (diag && key > q0 + j)) t = kNegInf;
-        x[j] = ex2(t);                                   // P^T
+      for (int j = 0; j < BQ; j += 2) {
+        const float4 st = rs4[j >> 1];
+        fma2(x[j], x[j + 1], x[j], x[j + 1], sc, sc, st.x, st.z);
       }
+      if (p.mask && key < p.S) {
+        const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(q0) * p.S + key;
+#pragma unroll
+        for (int j = 0; j < BQ; ++j)
+          if (q0 + j < p.L) x[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, x[j]);
+      }
+      if (key >= p.S) {
+#pragma unroll
+        for (int j = 0; j < BQ; ++j) x[j] = kNegInf;
+      } else if (p.causal && k0 + BKV - 1 > q0) {
+#pragma unroll
+        for (int j = 0; j < BQ; ++j)
+          if (key > q0 + j) x[j] = kNegInf;
+      }
+#pragma unroll
+      for (int j = 0; j < BQ; ++j) x[j] = ex2(x[j]);     // P^T
       mbar_wait(dp_full, i & 1, abort_flag, p.status, status_code(0x3a));
       tc_fence_after();
       float d[BQ];
@@ -342,23 +369,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(dp_free);
 #pragma unroll
-      for (int j = 0; j < BQ; ++j) d[j] = x[j] * (d[j] - rs[j].y);   // dS^T
-      if (i > 0) mbar_wait(p_free, (i - 1) & 1, abort_flag, p.status, status_code(0x3b));
+      for (int j = 0; j < BQ; j += 2) {                   // dS^T = P^T (dP^T - D)
+        const float4 st = rs4[j >> 1];
+        float t0, t1;
+        add2(t0, t1, d[j], d[j + 1], -st.y, -st.w);
+        mul2(d[j], d[j + 1], x[j], x[j + 1], t0, t1);
+      }
+      uint32_t pp[BQ / 2], pd[BQ / 2];
+#pragma unroll
+      for (int c = 0; c < BQ / 2; ++c) {
+        pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
+        pd[c] = pack_bf16x2(d[2 * c], d[2 * c + 1]);
+      }
+      if (i > 0) {
+        mbar_wait(p_free, (i - 1) & 1, abort_flag, p.status, status_code(0x3b));
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_off + kColP, pp);
+      tmem_st32(tmem + lane_off + kColDS, pd);
 #pragma unroll
       for (int c = 0; c < BQ / 8; ++c) {
-        uint4 w, u;
-        w.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
-        w.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
-        w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
-        w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
-        u.x = pack_bf16x2(d[8 * c + 0], d[8 * c + 1]);
-        u.y = pack_bf16x2(d[8 * c + 2], d[8 * c + 3]);
-        u.z = pack_bf16x2(d[8 * c + 4], d[8 * c + 5]);
-        u.w = pack_bf16x2(d[8 * c + 6], d[8 * c + 7]);
-        const int off = (c ^ (r & 7)) << 4;
-        *reinterpret_cast<uint4*>(prow + off) = w;
-        *reinterpret_cast<uint4*>(dsrow + off) = u;
+        const uint4 u = make_uint4(pd[4 * c], pd[4 * c + 1], pd[4 * c + 2], pd[4 * c + 3]);
+        *reinterpret_cast<uint4*>(dsrow + ((c ^ (r & 7)) << 4)) = u;
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -374,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const uint32_t col = m == 0 ? kColDK : kColDV;
-      const float sc = m == 0 ? p.scale : 1.f;
+      const float sc2 = m == 0 ? p.scale : 1.f;
       __nv_bfloat16* dst = m == 0 ? dkrow : dvrow;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -389,19 +423,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[u * 8 + 0]) * sc, __uint_as_float(v[u * 8 + 1]) * sc);
-            w.y = pack_bf16x2(__uint_as_float(v[u * 8 + 2]) * sc, __uint_as_float(v[u * 8 + 3]) * sc);
-            w.z = pack_bf16x2(__uint_as_float(v[u * 8 + 4]) * sc, __uint_as_float(v[u * 8 + 5]) * sc);
-            w.w = pack_bf16x2(__uint_as_float(v[u * 8 + 6]) * sc, __uint_as_float(v[u * 8 + 7]) * sc);
+            w.x = pack_bf16x2(__uint_as_float(v[u * 8 + 0]) * sc2, __uint_as_float(v[u * 8 + 1]) * sc2);
+            w.y = pack_bf16x2(__uint_as_float(v[u * 8 + 2]) * sc2, __uint_as_float(v[u * 8 + 3]) * sc2);
+            w.z = pack_bf16x2(__uint_as_float(v[u * 8 + 4]) * sc2, __uint_as_float(v[u * 8 + 5]) * sc2);
+            w.w = pack_bf16x2(__uint_as_float(v[u * 8 + 6]) * sc2, __uint_as_float(v[u * 8 + 7]) * sc2);
             *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = w;
           }
         }
       }
     }
   } else {
+    regs_inc<kRegsDrain>();
     // ------------------------------------------------------------ dQ drain (thread = head dim)
     const int e = (warp - 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    float* stage_dq = reinterpret_cast<float*>(smem + kOffDQ);
     for (int i = 0; i < n; ++i) {
       int qt, g;
       tile_of(i, qt, g);
@@ -415,15 +451,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free);
-      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.L + q0) * E + e;
-      const int nq = min(BQ, p.L - q0);
+      // the previous bulk reduction must have finished reading the staging rows
+      if (e == 0) bulk_wait_read_all();
+      named_bar(1, 128);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nq) red_add_f32(dst + static_cast<size_t>(j) * E, __uint_as_float(v0[j]) * p.scale);
+      for (int j = 0; j < 32; ++j) stage_dq[j * E + e] = __uint_as_float(v0[j]) * p.scale;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (32 + j < nq) red_add_f32(dst + static_cast<size_t>(32 + j) * E, __uint_as_float(v1[j]) * p.scale);
+      for (int j = 0; j < 32; ++j) stage_dq[(32 + j) * E + e] = __uint_as_float(v1[j]) * p.scale;
+      fence_proxy_async_smem();
+      named_bar(1, 128);
+      if (e == 0) {
+        const int nq = min(BQ, p.L - q0);
+        bulk_reduce_add_f32(p.dq_acc + (static_cast<size_t>(bh) * p.L + q0) * E, stage_dq,
+                            static_cast<uint32_t>(nq) * E * 4);
+        bulk_commit();
+      }
     }
+    if (e == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -444,9 +488,14 @@ cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st) {
   a.p = p;
   a.Lpad = (p.L + BQ - 1) / BQ * BQ;
   a.rowstats = reinterpret_cast<const float2*>(p.D);
+  // The register split in the main kernel assumes the launch reserves exactly kRegsLaunch per thread.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, bwd_tc_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const long long srows = static_cast<long long>(p.B) * p.Hq * a.Lpad;
   bwd_rowstats_kernel<<<static_cast<unsigned>((srows + 7) / 8), 256, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap tmK, tmV, tmQ, tmdO;
   if (!encode_tmap_bf16_3d(&tmK, p.k, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||

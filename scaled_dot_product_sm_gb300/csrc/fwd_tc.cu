@@ -6,11 +6,14 @@
 // 128-key tile at a time with a running max and sum (online softmax).
 //
 // One CTA = one (batch, query head) and two 128-row query tiles (256 rows)
-// that share every K/V tile load.  Warp roles (320 threads):
+// that share every K/V tile load.  Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax of query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through a ring
 //   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 10-11 idle (they complete the third warpgroup)
+// The third warpgroup hands registers to the softmax warpgroups (56 -> 224 per
+// thread: 4*32*56 + 8*32*224 = 64512 = 384*168, the launch's register file share).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+Ev), O_1 [384,384+Ev).
 // The softmax writes P_t as bf16 pairs over the first 64 columns of S_t, and
 // O_t += P_t V reads it straight from TMEM (A operand in TMEM), so P never
@@ -37,7 +40,12 @@ using namespace sdpa_ptx;
 
 constexpr int BM = 128;        // query rows per tile (MMA M)
 constexpr int BN = 128;        // keys per tile (MMA N of S, K of PV)
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168;   // registers per thread the kernel is compiled and launched with
+constexpr int kRegsSoftmax = 224;  // after setmaxnreg.inc (warpgroups 0 and 1)
+constexpr int kRegsOther = 56;     // after setmaxnreg.dec (warpgroup 2)
+static_assert(8 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther <= kThreads * kRegsLaunch, "register split too large");
+static_assert(2 * kRegsSoftmax + kRegsOther <= 512, "per sub-partition register file exceeded");
 constexpr int kChunkBytes = 128 * 128;   // one [128 rows x 64 bf16] swizzled block
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -121,10 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 8) {
+  if (warp >= 8) {
+    regs_dec<kRegsOther>();
+    if (warp == 8 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -152,10 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         load(false, j);
         if (j + 1 < n) load(true, j + 1);
       }
-    }
-  } else if (warp == 9) {
+    } else if (warp == 9 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);        // Q (K-major) x K (K-major)
       constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (TMEM, K-major) x V (MN-major)
       const uint32_t q_addr = smem_u32(smem + C::kOffQ);
@@ -218,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax warps
     const int t = warp >> 2;               // query tile
     const int wq = warp & 3;               // TMEM lane quarter
@@ -254,8 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int key = kb + 4 * c;
               if (key < p.S) {
                 const float4 mv = __ldg(reinterpret_cast<const float4*>(mrow + key));
-                fma2(x[4 * c + 0], x[4 * c + 1], mv.x, mv.y, kLog2e, kLog2e, x[4 * c + 0], x[4 * c + 1]);
-                fma2(x[4 * c + 2], x[4 * c + 3], mv.z, mv.w, kLog2e, kLog2e, x[4 * c + 2], x[4 * c + 3]);
+                x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
+                x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
+                x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
+                x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
               }
             }
           } else {
@@ -312,12 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t v[32];
               tmem_ld32(tO + c * 32, v);
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                float y0, y1;
-                mul2(y0, y1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), corr, corr);
-                v[i] = __float_as_uint(y0);
-                v[i + 1] = __float_as_uint(y1);
-              }
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
               tmem_st32(tO + c * 32, v);
             }
           }
@@ -380,7 +384,12 @@ cudaError_t run(const FwdParams& p, cudaStream_t st) {
       !encode_tmap_bf16_3d(&tmV, p.v, C::Ev, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BN))
     return cudaErrorInvalidValue;
   auto kern = fwd_tc_kernel<ECH, VCH>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  // The register split in the kernel assumes the launch reserves exactly kRegsLaunch per thread.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.Hq, (p.L + 2 * BM - 1) / (2 * BM));
   kern<<<grid, kThreads, C::kBytes, st>>>(tmQ, tmK, tmV, p);
