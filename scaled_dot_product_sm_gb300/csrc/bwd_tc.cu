@@ -25,11 +25,12 @@
 //     accumulator with one TMA bulk reduction per tile (the reduction runs in
 //     L2, full lines, one instruction);
 //  3. dQ = bf16(accumulator).
-// Warp roles (384 threads, three warpgroups with a register split):
-//   warps 0-3   elementwise (thread = key = TMEM lane)                 232 regs
-//   warps 4-7   dQ drain and staging (thread = head dim = TMEM lane)    216 regs
-//   warp  8     TMA producer, warp 9 TMEM allocator and MMA issuer,      56 regs
-//   warps 10-11 idle (they complete the third warpgroup)
+// Warp roles (512 threads, four warpgroups with a register split):
+//   warps 0-7   elementwise (thread = key = TMEM lane; warps w and w+4 share
+//               the lane quarter and take query columns 0-31 / 32-63)    152 regs
+//   warps 8-11  dQ drain and staging (thread = head dim = TMEM lane)     136 regs
+//   warp  12    TMA producer, warp 13 TMEM allocator and MMA issuer,      72 regs
+//   warps 14-15 idle (they complete the fourth warpgroup)
 // TMEM (512 columns): dK [0,128), dV [128,256), S^T [256,320), dP^T [320,384),
 // dQ^T [384,448), P^T bf16 [448,480), dS^T bf16 [480,512).
 // S^T(i+1) and dP^T(i+1) are issued as soon as the elementwise warps have read
@@ -51,14 +52,15 @@ using namespace sdpa_ptx;
 constexpr int E = 128, Ev = 128;
 constexpr int BKV = 128;       // keys per CTA
 constexpr int BQ = 64;         // queries per iteration
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kNSQ = 3;        // query-tile stages (prefetch two tiles ahead)
 constexpr float kNegInf = -__builtin_huge_valf();
 
-constexpr int kRegsLaunch = 168;
-constexpr int kRegsElem = 232, kRegsDrain = 216, kRegsOther = 56;
-static_assert(128 * (kRegsElem + kRegsDrain + kRegsOther) <= kThreads * kRegsLaunch, "register split too large");
-static_assert(kRegsElem + kRegsDrain + kRegsOther <= 512, "per sub-partition register file exceeded");
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsElem = 152, kRegsDrain = 136, kRegsOther = 72;
+static_assert(128 * (2 * kRegsElem + kRegsDrain + kRegsOther) <= kThreads * kRegsLaunch, "register split too large");
+static_assert(2 * kRegsElem + kRegsDrain + kRegsOther <= 512, "per sub-partition register file exceeded");
+constexpr int kHalf = BQ / 2;   // query columns per elementwise warp
 
 // shared memory map (bytes; every operand block 1024-aligned)
 constexpr int kKBytes = 2 * BKV * 128;                 // K tile: 2 chunks of [128 keys x 64 dims]
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO, TcBwdArgs a) {
   const BwdParams& p = a.p;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* kv_full = bar;                 // 1
   uint64_t* q_full = bar + 1;              // kNSQ
@@ -177,10 +179,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the group's heads innermost.  Every CTA of a KV group starts at the same
   // (last) tile and walks down in step, so the CTAs running at the same time
   // read the same Q/dO tiles and mostly hit in L2.
-  auto tile_of = [&](int i, int& qt, int& g) {
-    qt = nqt - 1 - i / p.G;
-    g = i - (i / p.G) * p.G;
+  struct TileIter {   // (query tile, head) of iteration i, advanced without divisions
+    int qt, g, G;
+    __device__ void next() {
+      if (++g == G) {
+        g = 0;
+        --qt;
+      }
+    }
   };
+  const TileIter tile0{nqt - 1, 0, p.G};
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -189,10 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 4);     // one arrival per elementwise warp
+    mbar_init(s_free, 8);     // one arrival per elementwise warp
     mbar_init(dp_full, 1);
-    mbar_init(dp_free, 4);
-    mbar_init(p_full, 4);
+    mbar_init(dp_free, 8);
+    mbar_init(p_full, 8);
     mbar_init(p_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);    // one arrival per drain warp
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -209,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 8) {
+  if (warp >= 12) {
     regs_dec<kRegsOther>();
-    if (warp == 8 && lane == 0 && n > 0) {
+    if (warp == 12 && lane == 0 && n > 0) {
       // ---------------------------------------------------------- TMA producer
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -222,10 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + kOffK + c * BKV * 128, &tmK, kv_full, c * 64, k0, bkv);
         tma_load_3d(smem + kOffV + c * BKV * 128, &tmV, kv_full, c * 64, k0, bkv);
       }
-      for (int i = 0; i < n; ++i) {
+      TileIter ti = tile0;
+      for (int i = 0; i < n; ++i, ti.next()) {
         const int s = i % kNSQ;
-        int qt, g;
-        tile_of(i, qt, g);
+        const int qt = ti.qt, g = ti.g;
         const int bh = b * p.Hq + hkv * p.G + g;
         mbar_wait(&q_empty[s], ((i / kNSQ) & 1) ^ 1, abort_flag, p.status, status_code(0x31));
         uint8_t* st = smem + kOffStage + s * kStage;
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bulk_load(st + 2 * kQTile, a.rowstats + static_cast<size_t>(bh) * a.Lpad + qt * BQ, BQ * 8, &q_full[s]);
       }
-    } else if (warp == 9 && lane == 0 && n > 0) {
+    } else if (warp == 13 && lane == 0 && n > 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T: K-major x K-major
       constexpr uint32_t id_kv = idesc_bf16(BKV, E, 0, 1);     // dV, dK: TMEM (K-major) x MN-major
@@ -300,84 +308,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit(kdv_done);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     regs_inc<kRegsElem>();
     // ------------------------------------------------------------ elementwise warps (thread = key)
-    const int r = warp * 32 + lane;
+    const int wq = warp & 3, hf = warp >> 2;   // TMEM lane quarter, query-column half
+    const int r = wq * 32 + lane;
     const int key = k0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     uint8_t* dsrow = smem + kOffDS + r * 128;
     const float sc = p.scale_log2;
-    for (int i = 0; i < n; ++i) {
+    TileIter ti = tile0;
+    for (int i = 0; i < n; ++i, ti.next()) {
       const int s = i % kNSQ;
-      int qt, g;
-      tile_of(i, qt, g);
+      const int qt = ti.qt, g = ti.g;
       const int h = hkv * p.G + g;
       const int q0 = qt * BQ;
       const float4* rs4 = reinterpret_cast<const float4*>(smem + kOffStage + s * kStage + 2 * kQTile);
       mbar_wait(&q_full[s], (i / kNSQ) & 1, abort_flag, p.status, status_code(0x38));
       mbar_wait(s_full, i & 1, abort_flag, p.status, status_code(0x39));
       tc_fence_after();
-      float x[BQ];
+      const int qc = q0 + hf * kHalf;          // first query of this warp's columns
+      const float4* rsw = rs4 + hf * (kHalf / 2);
+      float x[kHalf];
       {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kColS, v);
+        tmem_ld32(tmem + lane_off + kColS + hf * kHalf, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
-        tmem_ld32(tmem + lane_off + kColS + 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(v[j]);
+        for (int j = 0; j < kHalf; ++j) x[j] = __uint_as_float(v[j]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
       // t = s alpha log2e - lse log2e  (rowstats hold (-lse log2e, D) per query: two queries per float4)
 #pragma unroll
-      for (int j = 0; j < BQ; j += 2) {
-        const float4 st = rs4[j >> 1];
+      for (int j = 0; j < kHalf; j += 2) {
+        const float4 st = rsw[j >> 1];
         fma2(x[j], x[j + 1], x[j], x[j + 1], sc, sc, st.x, st.z);
       }
       if (p.mask && key < p.S) {
-        const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(q0) * p.S + key;
+        const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(qc) * p.S + key;
 #pragma unroll
-        for (int j = 0; j < BQ; ++j)
-          if (q0 + j < p.L) x[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, x[j]);
+        for (int j = 0; j < kHalf; ++j)
+          if (qc + j < p.L) x[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, x[j]);
       }
       if (key >= p.S) {
 #pragma unroll
-        for (int j = 0; j < BQ; ++j) x[j] = kNegInf;
-      } else if (p.causal && k0 + BKV - 1 > q0) {
+        for (int j = 0; j < kHalf; ++j) x[j] = kNegInf;
+      } else if (p.causal && k0 + BKV - 1 > qc) {
 #pragma unroll
-        for (int j = 0; j < BQ; ++j)
-          if (key > q0 + j) x[j] = kNegInf;
+        for (int j = 0; j < kHalf; ++j)
+          if (key > qc + j) x[j] = kNegInf;
       }
 #pragma unroll
-      for (int j = 0; j < BQ; ++j) x[j] = ex2(x[j]);     // P^T
+      for (int j = 0; j < kHalf; ++j) x[j] = ex2(x[j]);     // P^T
       mbar_wait(dp_full, i & 1, abort_flag, p.status, status_code(0x3a));
       tc_fence_after();
-      float d[BQ];
+      float d[kHalf];
       {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kColDP, v);
+        tmem_ld32(tmem + lane_off + kColDP + hf * kHalf, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]);
-        tmem_ld32(tmem + lane_off + kColDP + 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) d[32 + j] = __uint_as_float(v[j]);
+        for (int j = 0; j < kHalf; ++j) d[j] = __uint_as_float(v[j]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dp_free);
 #pragma unroll
-      for (int j = 0; j < BQ; j += 2) {                   // dS^T = P^T (dP^T - D)
-        const float4 st = rs4[j >> 1];
+      for (int j = 0; j < kHalf; j += 2) {                // dS^T = P^T (dP^T - D)
+        const float4 st = rsw[j >> 1];
         float t0, t1;
         add2(t0, t1, d[j], d[j + 1], -st.y, -st.w);
         mul2(d[j], d[j + 1], x[j], x[j + 1], t0, t1);
       }
-      uint32_t pp[BQ / 2], pd[BQ / 2];
+      uint32_t pp[kHalf / 2], pd[kHalf / 2];
 #pragma unroll
-      for (int c = 0; c < BQ / 2; ++c) {
+      for (int c = 0; c < kHalf / 2; ++c) {
         pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
         pd[c] = pack_bf16x2(d[2 * c], d[2 * c + 1]);
       }
@@ -385,12 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(p_free, (i - 1) & 1, abort_flag, p.status, status_code(0x3b));
         tc_fence_after();
       }
-      tmem_st32(tmem + lane_off + kColP, pp);
-      tmem_st32(tmem + lane_off + kColDS, pd);
+      tmem_st16(tmem + lane_off + kColP + hf * (kHalf / 2), pp);
+      tmem_st16(tmem + lane_off + kColDS + hf * (kHalf / 2), pd);
 #pragma unroll
-      for (int c = 0; c < BQ / 8; ++c) {
+      for (int c = 0; c < kHalf / 8; ++c) {
+        const int chunk = hf * (kHalf / 8) + c;
         const uint4 u = make_uint4(pd[4 * c], pd[4 * c + 1], pd[4 * c + 2], pd[4 * c + 3]);
-        *reinterpret_cast<uint4*>(dsrow + ((c ^ (r & 7)) << 4)) = u;
+        *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (r & 7)) << 4)) = u;
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -398,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // ---------------------------------------------------------- dK, dV epilogue
+    // ---------------------------------------------------------- dK, dV epilogue (one column half writes)
+    if (hf == 0) {
     __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bkv) * p.S + key) * E;
     __nv_bfloat16* dvrow = static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bkv) * p.S + key) * Ev;
     if (n > 0) {
@@ -432,15 +439,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+    }
+  } else if (warp < 12) {
     regs_inc<kRegsDrain>();
     // ------------------------------------------------------------ dQ drain (thread = head dim)
-    const int e = (warp - 4) * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const int e = (warp - 8) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 8) * 32) << 16;
     float* stage_dq = reinterpret_cast<float*>(smem + kOffDQ);
-    for (int i = 0; i < n; ++i) {
-      int qt, g;
-      tile_of(i, qt, g);
+    TileIter ti = tile0;
+    for (int i = 0; i < n; ++i, ti.next()) {
+      const int qt = ti.qt, g = ti.g;
       const int bh = b * p.Hq + hkv * p.G + g;
       const int q0 = qt * BQ;
       mbar_wait(dq_full, i & 1, abort_flag, p.status, status_code(0x3d));
@@ -471,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

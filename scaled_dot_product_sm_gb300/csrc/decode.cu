@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
   constexpr int kMt = Ev / 16;    // MMA m-tiles over Ev
   const FwdParams& p = dp.f;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSTAGE * SM::kStageBytes);
   uint64_t* empty = full + NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSTAGE);

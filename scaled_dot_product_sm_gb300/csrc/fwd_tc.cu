@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = FwdCfg<ECH, VCH>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* bar_q = bar;                 // 1
   uint64_t* full = bar + 1;              // NS
