@@ -249,23 +249,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T: K-major x K-major
       constexpr uint32_t id_kv = idesc_bf16(BKV, E, 0, 1);     // dV, dK: TMEM (K-major) x MN-major
       constexpr uint32_t id_q = idesc_bf16(E, BQ, 1, 1);       // dQ^T: MN-major x MN-major
-      const uint32_t kA = smem_u32(smem + kOffK), vA = smem_u32(smem + kOffV);
-      const uint32_t dsA = smem_u32(smem + kOffDS);
+      // Operand descriptors, built once; a K-step or a stage moves only the start address.
       const uint32_t stage0 = smem_u32(smem + kOffStage);
+      const SmemDesc dK_k = smem_desc(smem_u32(smem + kOffK), 16, 1024);            // K [keys x dims], K-major
+      const SmemDesc dV_k = smem_desc(smem_u32(smem + kOffV), 16, 1024);            // V [keys x dims], K-major
+      const SmemDesc dK_mn = smem_desc(smem_u32(smem + kOffK), BKV * 128, 1024);    // K^T as MN-major A
+      const SmemDesc dDS_mn = smem_desc(smem_u32(smem + kOffDS), BQ * 128, 1024);   // dS^T as MN-major B
+      const SmemDesc dQ_k = smem_desc(stage0, 16, 1024);                           // Q/dO stage 0, K-major
+      const SmemDesc dQ_mn = smem_desc(stage0, BQ * 128, 1024);                    // Q/dO stage 0, MN-major
       mbar_wait(kv_full, 0, abort_flag, p.status, status_code(0x32));
       auto issue_sdp = [&](int i) {
         const int s = i % kNSQ;
         mbar_wait(&q_full[s], (i / kNSQ) & 1, abort_flag, p.status, status_code(0x33));
         tc_fence_after();
-        const uint32_t qA = stage0 + s * kStage, doA = qA + kQTile;
+        const SmemDesc q_k = dQ_k + s * kStage, do_k = q_k + kQTile;
         if (i > 0) {
           mbar_wait(s_free, (i - 1) & 1, abort_flag, p.status, status_code(0x34));
           tc_fence_after();
         }
 #pragma unroll
         for (int kk = 0; kk < E / 16; ++kk) {
-          umma_ss(tmem + kColS, sdesc_sw128(kA + (kk >> 2) * (BKV * 128) + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(qA + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+          const uint32_t ka = (kk >> 2) * (BKV * 128) + (kk & 3) * 32, kb = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          umma_ss(tmem + kColS, dK_k + ka, q_k + kb, id_s, kk > 0);
         }
         umma_commit(s_full);
         if (i > 0) {
@@ -274,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int kk = 0; kk < Ev / 16; ++kk) {
-          umma_ss(tmem + kColDP, sdesc_sw128(vA + (kk >> 2) * (BKV * 128) + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(doA + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+          const uint32_t ka = (kk >> 2) * (BKV * 128) + (kk & 3) * 32, kb = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          umma_ss(tmem + kColDP, dV_k + ka, do_k + kb, id_s, kk > 0);
         }
         umma_commit(dp_full);
       };
@@ -283,15 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n; ++i) {
         if (i + 1 < n) issue_sdp(i + 1);
         const int s = i % kNSQ;
-        const uint32_t qA = stage0 + s * kStage, doA = qA + kQTile;
+        const SmemDesc q_mn = dQ_mn + s * kStage, do_mn = q_mn + kQTile;
         mbar_wait(p_full, i & 1, abort_flag, p.status, status_code(0x36));
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {   // dV += P^T dO ; dK += dS^T Q   (K = queries; 16 = 8 cols)
-          umma_ts(tmem + kColDV, tmem + kColP + kk * 8, sdesc_sw128(doA + kk * 16 * 128, BQ * 128, 1024), id_kv,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-          umma_ts(tmem + kColDK, tmem + kColDS + kk * 8, sdesc_sw128(qA + kk * 16 * 128, BQ * 128, 1024), id_kv,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + kColDV, tmem + kColP + kk * 8, do_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + kColDK, tmem + kColDS + kk * 8, q_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&q_empty[s]);
         if (i > 0) {
@@ -299,10 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
         }
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {  // dQ^T = K^T dS^T   (K = keys)
-          umma_ss(tmem + kColDQ, sdesc_sw128(kA + kk * 16 * 128, BKV * 128, 1024),
-                  sdesc_sw128(dsA + kk * 16 * 128, BQ * 128, 1024), id_q, kk > 0);
-        }
+        for (int kk = 0; kk < BKV / 16; ++kk)    // dQ^T = K^T dS^T   (K = keys)
+          umma_ss(tmem + kColDQ, dK_mn + kk * 16 * 128, dDS_mn + kk * 16 * 128, id_q, kk > 0);
         umma_commit(p_free);
         umma_commit(dq_full);
       }

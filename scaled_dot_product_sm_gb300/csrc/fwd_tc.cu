@@ -5,15 +5,18 @@
 // sections 2.1-2.2; stats as on the cuDNN "Attention" page), computed one
 // 128-key tile at a time with a running max and sum (online softmax).
 //
-// One CTA = one (batch, query head) and two 128-row query tiles (256 rows)
-// that share every K/V tile load.  Warp roles (384 threads, three warpgroups):
+// A work unit = one (batch, query head) and two 128-row query tiles (256 rows)
+// that share every K/V tile load.  The grid is persistent (one CTA per SM, each
+// walking a list of units), so the next unit's Q load and first scores overlap
+// the current unit's last tiles and epilogue.  Warp roles (384 threads, three
+// warpgroups):
 //   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax of query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through a ring
 //   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
 //   warps 10-11 idle (they complete the third warpgroup)
-// The third warpgroup hands registers to the softmax warpgroups (56 -> 224 per
-// thread: 4*32*56 + 8*32*224 = 64512 = 384*168, the launch's register file share).
+// The third warpgroup hands registers to the softmax warpgroups (72 -> 216 per
+// thread: 4*32*72 + 8*32*216 = 64512 = 384*168, the launch's register file share).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+Ev), O_1 [384,384+Ev).
 // The softmax writes P_t as bf16 pairs over the first 64 columns of S_t, and
 // O_t += P_t V reads it straight from TMEM (A operand in TMEM), so P never
@@ -42,8 +45,8 @@ constexpr int BM = 128;        // query rows per tile (MMA M)
 constexpr int BN = 128;        // keys per tile (MMA N of S, K of PV)
 constexpr int kThreads = 384;
 constexpr int kRegsLaunch = 168;   // registers per thread the kernel is compiled and launched with
-constexpr int kRegsSoftmax = 224;  // after setmaxnreg.inc (warpgroups 0 and 1)
-constexpr int kRegsOther = 56;     // after setmaxnreg.dec (warpgroup 2)
+constexpr int kRegsSoftmax = 216;  // after setmaxnreg.inc (warpgroups 0 and 1)
+constexpr int kRegsOther = 72;     // after setmaxnreg.dec (warpgroup 2)
 static_assert(8 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther <= kThreads * kRegsLaunch, "register split too large");
 static_assert(2 * kRegsSoftmax + kRegsOther <= 512, "per sub-partition register file exceeded");
 constexpr int kChunkBytes = 128 * 128;   // one [128 rows x 64 bf16] swizzled block
@@ -80,35 +83,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* bar_q = bar;                 // 1
-  uint64_t* full = bar + 1;              // NS
+  uint64_t* bar_q = bar;                 // 1: the unit's Q tiles landed
+  uint64_t* q_free = bar + 1;            // 1: every S MMA of the previous unit complete (Q buffers free)
+  uint64_t* full = bar + 2;              // NS
   uint64_t* empty = full + NS;           // NS
   uint64_t* s_full = empty + NS;         // 2: S_t(j) (and PV_t(j-1)) complete
   uint64_t* p_full = s_full + 2;         // 2: P_t(j) in TMEM (one arrival per warp)
-  uint64_t* o_final = p_full + 2;        // 2: the last PV_t complete
+  uint64_t* o_final = p_full + 2;        // 2: the last PV_t of the unit complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x, b = bh / p.Hq, h = bh - b * p.Hq;
-  const int bkv = b * p.Hkv + h / p.G;
-  const int unit = gridDim.y - 1 - blockIdx.y;      // longest (causal) units first
-  const int r0 = unit * 2 * BM;
-  int n_t[2];
+  // Work units: (batch x query head, pair of 128-row query tiles), listed heaviest
+  // first (causal: the last row pairs see the most key tiles).  The CTAs are
+  // persistent; CTA c takes units c, 2G-1-c, 2G+c, ... of the list (G CTAs),
+  // a snake order that evens out the causal work.
+  const int BHq = p.B * p.Hq;
+  const int units = (p.L + 2 * BM - 1) / (2 * BM);
+  const int total = BHq * units;
+  auto unit_index = [&](int r) {   // r-th unit of this CTA, or -1
+    const int G = gridDim.x, c = blockIdx.x;
+    const int k = r * G + ((r & 1) ? G - 1 - c : c);
+    return k < total ? k : -1;
+  };
+  struct Unit {
+    int bh, b, h, bkv, r0, n_t[2], n;
+  };
+  auto unit_at = [&](int k) {
+    Unit u;
+    const int pair = k / BHq;
+    u.bh = k - pair * BHq;
+    u.b = u.bh / p.Hq;
+    u.h = u.bh - u.b * p.Hq;
+    u.bkv = u.b * p.Hkv + u.h / p.G;
+    u.r0 = (units - 1 - pair) * 2 * BM;
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int rt = r0 + t * BM;
-    if (rt >= p.L) {
-      n_t[t] = 0;
-    } else {
-      const int kmax = p.causal ? min(p.S, rt + BM) : p.S;
-      n_t[t] = (kmax + BN - 1) / BN;
+    for (int t = 0; t < 2; ++t) {
+      const int rt = u.r0 + t * BM;
+      if (rt >= p.L) {
+        u.n_t[t] = 0;
+      } else {
+        const int kmax = p.causal ? min(p.S, rt + BM) : p.S;
+        u.n_t[t] = (kmax + BN - 1) / BN;
+      }
     }
-  }
-  const int n = max(n_t[0], n_t[1]);   // n_t[0] <= n_t[1] unless tile 1 is past L
+    u.n = max(u.n_t[0], u.n_t[1]);   // n_t[0] <= n_t[1] unless tile 1 is past L
+    return u;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
+    mbar_init(q_free, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -136,91 +161,110 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      const int nq = (n_t[0] > 0) + (n_t[1] > 0);
-      mbar_arrive_expect_tx(bar_q, nq * C::kQBytes);
-      for (int t = 0; t < 2; ++t) {
-        if (n_t[t] == 0) continue;
-        for (int c = 0; c < ECH; ++c)
-          tma_load_3d(smem + C::kOffQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar_q, c * 64, r0 + t * BM, bh);
-      }
-      // ring order = consumption order: K_0, then per j: V_j, K_{j+1} (if any)
-      int it = 0;
-      auto load = [&](bool is_k, int j) {
-        const int s = it % NS;
-        mbar_wait(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.status, status_code(0x11));
-        uint8_t* dst = smem + C::kOffRing + s * C::kItem;
-        const int ch = is_k ? ECH : VCH;
-        mbar_arrive_expect_tx(&full[s], ch * kChunkBytes);
-        for (int c = 0; c < ch; ++c)
-          tma_load_3d(dst + c * kChunkBytes, is_k ? &tmK : &tmV, &full[s], c * 64, j * BN, bkv);
-        ++it;
-      };
-      load(true, 0);
-      for (int j = 0; j < n; ++j) {
-        load(false, j);
-        if (j + 1 < n) load(true, j + 1);
+      int it = 0;   // ring position, continued across units
+      for (int r = 0;; ++r) {
+        const int k = unit_index(r);
+        if (k < 0) break;
+        const Unit u = unit_at(k);
+        // the previous unit's S MMAs have read its Q tiles
+        mbar_wait(q_free, (r & 1) ^ 1, abort_flag, p.status, status_code(0x10));
+        const int nq = (u.n_t[0] > 0) + (u.n_t[1] > 0);
+        mbar_arrive_expect_tx(bar_q, nq * C::kQBytes);
+        for (int t = 0; t < 2; ++t) {
+          if (u.n_t[t] == 0) continue;
+          for (int c = 0; c < ECH; ++c)
+            tma_load_3d(smem + C::kOffQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar_q, c * 64, u.r0 + t * BM,
+                        u.bh);
+        }
+        // ring order = consumption order: K_0, then per j: V_j, K_{j+1} (if any)
+        auto load = [&](bool is_k, int j) {
+          const int s = it % NS;
+          mbar_wait(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.status, status_code(0x11));
+          uint8_t* dst = smem + C::kOffRing + s * C::kItem;
+          const int ch = is_k ? ECH : VCH;
+          mbar_arrive_expect_tx(&full[s], ch * kChunkBytes);
+          for (int c = 0; c < ch; ++c)
+            tma_load_3d(dst + c * kChunkBytes, is_k ? &tmK : &tmV, &full[s], c * 64, j * BN, u.bkv);
+          ++it;
+        };
+        load(true, 0);
+        for (int j = 0; j < u.n; ++j) {
+          load(false, j);
+          if (j + 1 < u.n) load(true, j + 1);
+        }
       }
     } else if (warp == 9 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);        // Q (K-major) x K (K-major)
       constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (TMEM, K-major) x V (MN-major)
-      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
-      const uint32_t ring = smem_u32(smem + C::kOffRing);
-      auto issue_s = [&](int t, uint32_t kaddr) {
-        const uint32_t qa = q_addr + t * C::kQBytes;
+      // Operand descriptors, built once; a K-step, a tile or a ring slot moves only the start address.
+      const SmemDesc dq = smem_desc(smem_u32(smem + C::kOffQ), 16, 1024);            // Q, K-major
+      const SmemDesc dk = smem_desc(smem_u32(smem + C::kOffRing), 16, 1024);         // K slot 0, K-major
+      const SmemDesc dv = smem_desc(smem_u32(smem + C::kOffRing), kChunkBytes, 1024);  // V slot 0, MN-major
+      auto issue_s = [&](int t, int slot) {
+        const SmemDesc qa = dq + t * C::kQBytes, ka = dk + slot * C::kItem;
 #pragma unroll
         for (int kk = 0; kk < C::E / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          umma_ss(tmem + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024), idesc_s,
-                  kk > 0);
+          umma_ss(tmem + t * BN, qa + off, ka + off, idesc_s, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const SmemDesc va = dv + slot * C::kItem;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 8 TMEM columns of bf16 pairs per step
-          umma_ts(tmem + 256 + t * 128, tmem + t * BN + kk * 8,
-                  sdesc_sw128(vaddr + kk * 16 * 128, kChunkBytes, 1024), idesc_o, (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + 256 + t * 128, tmem + t * BN + kk * 8, va + kk * 16 * 128, idesc_o,
+                  (acc || kk > 0) ? 1u : 0u);
       };
-      mbar_wait(bar_q, 0, abort_flag, p.status, status_code(0x12));
-      int it = 0;
-      {
-        const int s = it % NS;
-        mbar_wait(&full[s], (it / NS) & 1, abort_flag, p.status, status_code(0x13));
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (n_t[t] == 0) continue;
-          issue_s(t, ring + s * C::kItem);
-          umma_commit(&s_full[t]);
-        }
-        umma_commit(&empty[s]);
-        ++it;
-      }
-      for (int j = 0; j < n; ++j) {
-        const int sv = it % NS;
-        mbar_wait(&full[sv], (it / NS) & 1, abort_flag, p.status, status_code(0x14));
-        tc_fence_after();
-        ++it;
-        int sk = -1;
-        for (int t = 0; t < 2; ++t) {
-          if (j >= n_t[t]) continue;
-          mbar_wait(&p_full[t], j & 1, abort_flag, p.status, status_code(0x15));
+      int it = 0;               // ring position, continued across units
+      uint32_t pc[2] = {0, 0};  // p_full completions consumed per tile
+      for (int r = 0;; ++r) {
+        const int k = unit_index(r);
+        if (k < 0) break;
+        const Unit u = unit_at(k);
+        mbar_wait(bar_q, r & 1, abort_flag, p.status, status_code(0x12));
+        {
+          const int s = it % NS;
+          mbar_wait(&full[s], (it / NS) & 1, abort_flag, p.status, status_code(0x13));
           tc_fence_after();
-          issue_pv(t, ring + sv * C::kItem, j > 0);
-          if (j + 1 < n_t[t]) {
-            if (sk < 0) {
-              sk = it % NS;
-              mbar_wait(&full[sk], (it / NS) & 1, abort_flag, p.status, status_code(0x16));
-              tc_fence_after();
-              ++it;
-            }
-            issue_s(t, ring + sk * C::kItem);   // overwrites P_t(j) after PV_t(j) in issue order
+          for (int t = 0; t < 2; ++t) {
+            if (u.n_t[t] == 0) continue;
+            issue_s(t, s);
             umma_commit(&s_full[t]);
-          } else {
-            umma_commit(&o_final[t]);
           }
+          umma_commit(&empty[s]);
+          if (u.n == 1) umma_commit(q_free);
+          ++it;
         }
-        umma_commit(&empty[sv]);
-        if (sk >= 0) umma_commit(&empty[sk]);
+        for (int j = 0; j < u.n; ++j) {
+          const int sv = it % NS;
+          mbar_wait(&full[sv], (it / NS) & 1, abort_flag, p.status, status_code(0x14));
+          tc_fence_after();
+          ++it;
+          int sk = -1;
+          for (int t = 0; t < 2; ++t) {
+            if (j >= u.n_t[t]) continue;
+            mbar_wait(&p_full[t], pc[t] & 1, abort_flag, p.status, status_code(0x15));
+            ++pc[t];
+            tc_fence_after();
+            issue_pv(t, sv, j > 0);
+            if (j + 1 < u.n_t[t]) {
+              if (sk < 0) {
+                sk = it % NS;
+                mbar_wait(&full[sk], (it / NS) & 1, abort_flag, p.status, status_code(0x16));
+                tc_fence_after();
+                ++it;
+              }
+              issue_s(t, sk);   // overwrites P_t(j) after PV_t(j) in issue order
+              umma_commit(&s_full[t]);
+            } else {
+              umma_commit(&o_final[t]);
+            }
+          }
+          umma_commit(&empty[sv]);
+          if (sk >= 0) umma_commit(&empty[sk]);
+          if (j + 2 == u.n) umma_commit(q_free);   // the unit's last S MMAs were just issued
+        }
       }
     }
   } else {
@@ -229,20 +273,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;               // query tile
     const int wq = warp & 3;               // TMEM lane quarter
     const int r = wq * 32 + lane;          // row within the tile = TMEM lane
-    const int row = r0 + t * BM + r;
-    const int nt = n_t[t];
-    if (nt > 0) {
-      const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-      const uint32_t tS = tmem + lane_off + t * BN;
-      const uint32_t tO = tmem + lane_off + 256 + t * 128;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * BN;
+    const uint32_t tO = tmem + lane_off + 256 + t * 128;
+    const float sc = p.scale_log2;
+    uint32_t sc_cnt = 0, oc_cnt = 0;       // s_full / o_final completions consumed
+    for (int ur = 0;; ++ur) {
+      const int k = unit_index(ur);
+      if (k < 0) break;
+      const Unit u = unit_at(k);
+      const int nt = u.n_t[t];
+      if (nt == 0) continue;
+      const int row_first = u.r0 + t * BM;   // first row of this tile
+      const int row = row_first + r;
       const float* mrow = (p.mask && row < p.L)
-                              ? p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(row) * p.S
+                              ? p.mask + u.b * p.mask_sb + u.h * p.mask_sh + static_cast<size_t>(row) * p.S
                               : nullptr;
-      const int row_first = r0 + t * BM;   // first row of this tile
-      const float sc = p.scale_log2;
       float m_run = kNegInf, l_run = 0.f;
       for (int j = 0; j < nt; ++j) {
-        mbar_wait(&s_full[t], j & 1, abort_flag, p.status, status_code(0x18));
+        mbar_wait(&s_full[t], sc_cnt & 1, abort_flag, p.status, status_code(0x18));
+        ++sc_cnt;
         tc_fence_after();
         float x[BN];
         {
@@ -286,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // row max: eight independent chains of three-input maxima
         float mx8[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(x[u], x[8 + u]);
+        for (int u8 = 0; u8 < 8; ++u8) mx8[u8] = fmaxf(x[u8], x[8 + u8]);
 #pragma unroll
         for (int i = 16; i < BN; i += 16)
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mx8[u] = max3f(mx8[u], x[i + u], x[i + 8 + u]);
+          for (int u8 = 0; u8 < 8; ++u8) mx8[u8] = max3f(mx8[u8], x[i + u8], x[i + 8 + u8]);
         const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
                                fmaxf(mx8[6], mx8[7]));
         const float m_new = fmaxf(m_run, mx);
@@ -307,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           add2(a0, a1, x[i], x[i + 1], nm, nm);
           a0 = ex2(a0);
           a1 = ex2(a1);
-          const int u = (i >> 1) & 3;
-          add2(rs8[2 * u], rs8[2 * u + 1], rs8[2 * u], rs8[2 * u + 1], a0, a1);
+          const int q4 = (i >> 1) & 3;
+          add2(rs8[2 * q4], rs8[2 * q4 + 1], rs8[2 * q4], rs8[2 * q4 + 1], a0, a1);
           pk[i >> 1] = pack_bf16x2(a0, a1);
         }
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
@@ -343,28 +393,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&p_full[t]);
       }
       // ---------------------------------------------------------- epilogue
-      mbar_wait(&o_final[t], 0, abort_flag, p.status, status_code(0x1a));
+      // O_t is read out before this warp writes the next unit's P_t, so the
+      // next unit's first PV_t (which waits for that P_t) cannot overwrite it early.
+      mbar_wait(&o_final[t], oc_cnt & 1, abort_flag, p.status, status_code(0x1a));
+      ++oc_cnt;
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.L + row) * C::Ev;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(u.bh) * p.L + row) * C::Ev;
 #pragma unroll
       for (int c = 0; c < C::Ev / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tO + c * 32, v);
         if (row < p.L) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[u * 8 + 0]) * inv, __uint_as_float(v[u * 8 + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(v[u * 8 + 2]) * inv, __uint_as_float(v[u * 8 + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(v[u * 8 + 4]) * inv, __uint_as_float(v[u * 8 + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(v[u * 8 + 6]) * inv, __uint_as_float(v[u * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) = w;
+            w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = w;
           }
         }
       }
       if (row < p.L)
-        p.lse[static_cast<size_t>(bh) * p.L + row] = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
+        p.lse[static_cast<size_t>(u.bh) * p.L + row] = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
+      tc_fence_before();
     }
   }
   tc_fence_before();
@@ -391,7 +445,11 @@ cudaError_t run(const FwdParams& p, cudaStream_t st) {
   if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.B * p.Hq, (p.L + 2 * BM - 1) / (2 * BM));
+  const long long units = static_cast<long long>(p.B) * p.Hq * ((p.L + 2 * BM - 1) / (2 * BM));
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);   // persistent: one CTA per SM
   kern<<<grid, kThreads, C::kBytes, st>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }

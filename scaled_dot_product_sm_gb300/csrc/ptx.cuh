@@ -256,6 +256,39 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor kept as two 32-bit halves: `lo` holds the start address
+// (bits 0-13, address >> 4) and the leading byte offset, `hi` the stride byte
+// offset, version and swizzle.  Moving the start address by a multiple of 16
+// bytes is one 32-bit add on `lo`: shared addresses are below 2^18, so the
+// address field never carries into the offset field.
+struct SmemDesc {
+  uint32_t lo, hi;
+  __device__ __forceinline__ SmemDesc operator+(uint32_t bytes) const { return SmemDesc{lo + (bytes >> 4), hi}; }
+};
+__device__ __forceinline__ SmemDesc smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  const uint64_t d = sdesc_sw128(saddr, lbo_bytes, sbo_bytes);
+  return SmemDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
 // M x N tile, a_mn / b_mn = 1 when that operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

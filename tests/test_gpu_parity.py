@@ -162,6 +162,9 @@ BF16_CASES = [
     (1, 8, 2, 100, 300, 128, 128, True, "none", None, 0),   # key tiles past every query: dK = dV = 0
     (2, 4, 1, 333, 333, 128, 128, True, "bias", (2, 4), 2), # GQA causal + per-head mask, ragged
     (1, 2, 2, 64, 1000, 128, 128, False, "block", (1, 2), 0),
+    # more work units than SMs: the persistent forward walks several units per CTA
+    (2, 96, 32, 300, 333, 128, 128, True, "bias", (2, 1), 2),
+    (1, 200, 200, 130, 140, 64, 64, False, "none", None, 0),
 ]
 
 
