@@ -9,9 +9,9 @@
 // (apply) and the FlashAttention-2 backward the chapter points to do.
 //
 // Three launches:
-//  1. rowstats: per query row (-lse*log2(e), D) as a float2 (rows padded to a
-//     multiple of 64 with (-inf, 0), so a padded or fully masked row has P = 0),
-//     and the fp32 dQ accumulator zeroed;
+//  1. rowstats: per 64-row query tile, the 64 values -lse*log2(e) followed by
+//     the 64 values -D (rows padded to a multiple of 64 with (-inf, 0), so a
+//     padded or fully masked row has P = 0), and the fp32 dQ accumulator zeroed;
 //  2. the main kernel, one CTA per (batch, KV head, 128-key tile).  K and V stay
 //     in shared memory; the CTA walks the Hq/Hkv query heads of its group and
 //     their 64-row query tiles (last to first, down to the diagonal when
@@ -21,21 +21,29 @@
 //        P^T  = exp2(S^T alpha log2e + mask log2e - lse log2e),  dS^T = P^T o (dP^T - D)
 //        dV  += P^T dO,  dK += dS^T Q       (A operands P^T, dS^T read from TMEM)
 //        dQ^T = K^T dS^T                    (TMEM, 128 head dims x 64 queries; dS^T also in smem)
-//     dQ^T is staged in shared memory as dQ rows and added to the global fp32
-//     accumulator with one TMA bulk reduction per tile (the reduction runs in
-//     L2, full lines, one instruction);
-//  3. dQ = bf16(accumulator).
+//     dQ^T is staged in shared memory as dQ rows and added (without alpha) to
+//     the global fp32 accumulator with one TMA bulk reduction per tile (the
+//     reduction runs in L2, full lines, one instruction);
+//  3. dQ = bf16(alpha * accumulator).
 // Warp roles (512 threads, four warpgroups with a register split):
 //   warps 0-7   elementwise (thread = key = TMEM lane; warps w and w+4 share
 //               the lane quarter and take query columns 0-31 / 32-63)    152 regs
 //   warps 8-11  dQ drain and staging (thread = head dim = TMEM lane)     136 regs
-//   warp  12    TMA producer, warp 13 TMEM allocator and MMA issuer,      72 regs
-//   warps 14-15 idle (they complete the fourth warpgroup)
+//   warp  12    TMA producer                                              72 regs
+//   warp  13    TMEM allocator and issuer of the gradient MMAs (dV, dK, dQ^T)
+//   warp  14    issuer of the score MMAs (S^T, dP^T)
+//   warp  15    idle (it completes the fourth warpgroup)
 // TMEM (512 columns): dK [0,128), dV [128,256), S^T [256,320), dP^T [320,384),
 // dQ^T [384,448), P^T bf16 [448,480), dS^T bf16 [480,512).
-// S^T(i+1) and dP^T(i+1) are issued as soon as the elementwise warps have read
-// S^T(i) and dP^T(i), so the tensor core computes the next scores while the
-// current gradients wait for P^T and dS^T.
+// Two threads issue MMAs into the one tensor pipe: the score issuer puts
+// S^T(i+1) and dP^T(i+1) in as soon as the elementwise warps have read S^T(i)
+// and dP^T(i), the gradient issuer puts dV, dK (i) in once P^T(i) and dS^T(i)
+// are stored.  The pipe accepts only a few MMAs ahead, so with one issuer every
+// barrier it waited on let the pipe run dry; with two, one thread's wait does
+// not stop the other's work.  The two streams touch disjoint TMEM columns and
+// everything that orders them goes through the elementwise warps' barriers
+// (the gradient MMAs of tile i start after P^T(i), which needs S^T(i) and
+// dP^T(i) complete), so each thread's commits only have to cover its own MMAs.
 #include <cuda.h>
 
 #include <algorithm>
@@ -97,7 +105,7 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 struct TcBwdArgs {
   BwdParams p;
-  const float2* rowstats;   // [B*Hq][Lpad] (-lse*log2e, D)
+  const float* rowstats;   // per (head, 64-row query tile): 64 x (-lse*log2e), then 64 x (-D)
   int Lpad;
 };
 
@@ -109,7 +117,7 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(TcBwdArgs a) {
   if (gr >= rows) return;
   const long long bh = gr / a.Lpad;
   const int q = static_cast<int>(gr - bh * a.Lpad);
-  float2 st = make_float2(kNegInf, 0.f);
+  float nl = kNegInf, nd = 0.f;
   if (q < p.L) {
     const size_t row = static_cast<size_t>(bh) * p.L + q;
     const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o) + row * Ev;
@@ -124,24 +132,30 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(TcBwdArgs a) {
     s = fmaf(__high2float(b2), __high2float(d2), s);
     s = warp_sum(s);
     const float lse = p.lse[row];
-    st = make_float2(lse == kNegInf ? kNegInf : -lse * kLog2e, s);
+    nl = lse == kNegInf ? kNegInf : -lse * kLog2e;
+    nd = -s;
     float4* acc = reinterpret_cast<float4*>(p.dq_acc + row * E);
     acc[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (lane == 0) const_cast<float2*>(a.rowstats)[gr] = st;
+  if (lane == 0) {
+    float* tile = const_cast<float*>(a.rowstats) + (gr - (q & (BQ - 1))) * 2;   // this row's 64-row tile
+    tile[q & (BQ - 1)] = nl;
+    tile[BQ + (q & (BQ - 1))] = nd;
+  }
 }
 
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p) {
+  const float sc = p.scale;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(p.dq_acc)[2 * i];
     const float4 b = reinterpret_cast<const float4*>(p.dq_acc)[2 * i + 1];
     uint4 w;
-    w.x = pack_bf16x2(a.x, a.y);
-    w.y = pack_bf16x2(a.z, a.w);
-    w.z = pack_bf16x2(b.x, b.y);
-    w.w = pack_bf16x2(b.z, b.w);
+    w.x = pack_bf16x2(a.x * sc, a.y * sc);
+    w.y = pack_bf16x2(a.z * sc, a.w * sc);
+    w.z = pack_bf16x2(b.x * sc, b.y * sc);
+    w.w = pack_bf16x2(b.z * sc, b.w * sc);
     reinterpret_cast<uint4*>(p.dq)[i] = w;
   }
 }
@@ -242,10 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(st + c * BQ * 128, &tmQ, &q_full[s], c * 64, qt * BQ, bh);
           tma_load_3d(st + kQTile + c * BQ * 128, &tmdO, &q_full[s], c * 64, qt * BQ, bh);
         }
-        bulk_load(st + 2 * kQTile, a.rowstats + static_cast<size_t>(bh) * a.Lpad + qt * BQ, BQ * 8, &q_full[s]);
+        bulk_load(st + 2 * kQTile, a.rowstats + (static_cast<size_t>(bh) * a.Lpad + qt * BQ) * 2, BQ * 8,
+                  &q_full[s]);
       }
-    } else if (warp == 13 && lane == 0 && n > 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if ((warp == 13 || warp == 14) && lane == 0 && n > 0) {
+      // ---------------------------------------------------------- MMA issuers
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T: K-major x K-major
       constexpr uint32_t id_kv = idesc_bf16(BKV, E, 0, 1);     // dV, dK: TMEM (K-major) x MN-major
       constexpr uint32_t id_q = idesc_bf16(E, BQ, 1, 1);       // dQ^T: MN-major x MN-major
@@ -284,30 +299,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(dp_full);
       };
-      issue_sdp(0);
-      for (int i = 0; i < n; ++i) {
-        if (i + 1 < n) issue_sdp(i + 1);
-        const int s = i % kNSQ;
-        const SmemDesc q_mn = dQ_mn + s * kStage, do_mn = q_mn + kQTile;
-        mbar_wait(p_full, i & 1, abort_flag, p.status, status_code(0x36));
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {   // dV += P^T dO ; dK += dS^T Q   (K = queries; 16 = 8 cols)
-          umma_ts(tmem + kColDV, tmem + kColP + kk * 8, do_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          umma_ts(tmem + kColDK, tmem + kColDS + kk * 8, q_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&q_empty[s]);
-        if (i > 0) {
-          mbar_wait(dq_free, (i - 1) & 1, abort_flag, p.status, status_code(0x37));
+      if (warp == 14) {
+        for (int i = 0; i < n; ++i) issue_sdp(i);   // score MMAs
+      } else {
+        for (int i = 0; i < n; ++i) {               // gradient MMAs
+          const int s = i % kNSQ;
+          const SmemDesc q_mn = dQ_mn + s * kStage, do_mn = q_mn + kQTile;
+          mbar_wait(p_full, i & 1, abort_flag, p.status, status_code(0x36));
           tc_fence_after();
-        }
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)    // dQ^T = K^T dS^T   (K = keys)
-          umma_ss(tmem + kColDQ, dK_mn + kk * 16 * 128, dDS_mn + kk * 16 * 128, id_q, kk > 0);
-        umma_commit(p_free);
-        umma_commit(dq_full);
+          for (int kk = 0; kk < BQ / 16; ++kk) {   // dV += P^T dO ; dK += dS^T Q   (K = queries; 16 = 8 cols)
+            umma_ts(tmem + kColDV, tmem + kColP + kk * 8, do_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tmem + kColDK, tmem + kColDS + kk * 8, q_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&q_empty[s]);
+          if (i > 0) {
+            mbar_wait(dq_free, (i - 1) & 1, abort_flag, p.status, status_code(0x37));
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk)    // dQ^T = K^T dS^T   (K = keys)
+            umma_ss(tmem + kColDQ, dK_mn + kk * 16 * 128, dDS_mn + kk * 16 * 128, id_q, kk > 0);
+          umma_commit(p_free);
+          umma_commit(dq_full);
+        }
+        umma_commit(kdv_done);
       }
-      umma_commit(kdv_done);
     }
   } else if (warp < 8) {
     regs_inc<kRegsElem>();
@@ -324,12 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = ti.qt, g = ti.g;
       const int h = hkv * p.G + g;
       const int q0 = qt * BQ;
-      const float4* rs4 = reinterpret_cast<const float4*>(smem + kOffStage + s * kStage + 2 * kQTile);
+      const float* rs = reinterpret_cast<const float*>(smem + kOffStage + s * kStage + 2 * kQTile);
+      const int qc = q0 + hf * kHalf;          // first query of this warp's columns
       mbar_wait(&q_full[s], (i / kNSQ) & 1, abort_flag, p.status, status_code(0x38));
+      // this warp's 32 values -lse*log2e, read before the scores arrive
+      float nl[kHalf];
+#pragma unroll
+      for (int c = 0; c < kHalf / 4; ++c) {
+        const float4 v4 = reinterpret_cast<const float4*>(rs + hf * kHalf)[c];
+        nl[4 * c] = v4.x, nl[4 * c + 1] = v4.y, nl[4 * c + 2] = v4.z, nl[4 * c + 3] = v4.w;
+      }
       mbar_wait(s_full, i & 1, abort_flag, p.status, status_code(0x39));
       tc_fence_after();
-      const int qc = q0 + hf * kHalf;          // first query of this warp's columns
-      const float4* rsw = rs4 + hf * (kHalf / 2);
       float x[kHalf];
       {
         uint32_t v[32];
@@ -340,28 +363,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
-      // t = s alpha log2e - lse log2e  (rowstats hold (-lse log2e, D) per query: two queries per float4)
+      // t = s alpha log2e - lse log2e
 #pragma unroll
-      for (int j = 0; j < kHalf; j += 2) {
-        const float4 st = rsw[j >> 1];
-        fma2(x[j], x[j + 1], x[j], x[j + 1], sc, sc, st.x, st.z);
+      for (int j = 0; j < kHalf; j += 2) fma2(x[j], x[j + 1], x[j], x[j + 1], sc, sc, nl[j], nl[j + 1]);
+      if (p.mask) {
+        if (key < p.S) {
+          const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(qc) * p.S + key;
+#pragma unroll
+          for (int j = 0; j < kHalf; ++j)
+            if (qc + j < p.L) x[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, x[j]);
+        }
       }
-      if (p.mask && key < p.S) {
-        const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(qc) * p.S + key;
+      // keys past S, and (causal) keys after the query: both tests are warp-uniform to skip
+      if (k0 + BKV > p.S || (p.causal && k0 + BKV - 1 > qc)) {
 #pragma unroll
         for (int j = 0; j < kHalf; ++j)
-          if (qc + j < p.L) x[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, x[j]);
-      }
-      if (key >= p.S) {
-#pragma unroll
-        for (int j = 0; j < kHalf; ++j) x[j] = kNegInf;
-      } else if (p.causal && k0 + BKV - 1 > qc) {
-#pragma unroll
-        for (int j = 0; j < kHalf; ++j)
-          if (key > qc + j) x[j] = kNegInf;
+          if (key >= p.S || (p.causal && key > qc + j)) x[j] = kNegInf;
       }
 #pragma unroll
       for (int j = 0; j < kHalf; ++j) x[j] = ex2(x[j]);     // P^T
+      float nd[kHalf];   // -D of this warp's 32 queries
+#pragma unroll
+      for (int c = 0; c < kHalf / 4; ++c) {
+        const float4 v4 = reinterpret_cast<const float4*>(rs + BQ + hf * kHalf)[c];
+        nd[4 * c] = v4.x, nd[4 * c + 1] = v4.y, nd[4 * c + 2] = v4.z, nd[4 * c + 3] = v4.w;
+      }
       mbar_wait(dp_full, i & 1, abort_flag, p.status, status_code(0x3a));
       tc_fence_after();
       float d[kHalf];
@@ -376,9 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(dp_free);
 #pragma unroll
       for (int j = 0; j < kHalf; j += 2) {                // dS^T = P^T (dP^T - D)
-        const float4 st = rsw[j >> 1];
         float t0, t1;
-        add2(t0, t1, d[j], d[j + 1], -st.y, -st.w);
+        add2(t0, t1, d[j], d[j + 1], nd[j], nd[j + 1]);
         mul2(d[j], d[j + 1], x[j], x[j + 1], t0, t1);
       }
       uint32_t pp[kHalf / 2], pd[kHalf / 2];
@@ -464,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (e == 0) bulk_wait_read_all();
       named_bar(1, 128);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) stage_dq[j * E + e] = __uint_as_float(v0[j]) * p.scale;
+      for (int j = 0; j < 32; ++j) stage_dq[j * E + e] = __uint_as_float(v0[j]);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) stage_dq[(32 + j) * E + e] = __uint_as_float(v1[j]) * p.scale;
+      for (int j = 0; j < 32; ++j) stage_dq[(32 + j) * E + e] = __uint_as_float(v1[j]);
       fence_proxy_async_smem();
       named_bar(1, 128);
       if (e == 0) {
@@ -496,7 +521,7 @@ cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st) {
   TcBwdArgs a;
   a.p = p;
   a.Lpad = (p.L + BQ - 1) / BQ * BQ;
-  a.rowstats = reinterpret_cast<const float2*>(p.D);
+  a.rowstats = p.D;
   // The register split in the main kernel assumes the launch reserves exactly kRegsLaunch per thread.
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, bwd_tc_kernel);
