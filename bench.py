@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--workload", default=MAIN,
+                    choices=["tiny_f32", "tiny_f32_causal", "mha_causal_e64", "gqa_causal_e128", "padded_mask_e128"],
+                    help="prefill workload of the step (default: the GQA causal E=128 headline workload)")
     ap.add_argument("--phase", choices=["all", "fwd", "bwd", "decode"], default="all",
                     help="profiling aid: run only the forward loop, the backward loop or the decode leg")
     ap.add_argument("--summarize-launches", metavar="CSV",
@@ -205,23 +208,26 @@ def run_ours(args, ws, rank, local):
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
 
-    w = workloads.get(MAIN)
-    q_h, k_h, v_h, dO_h, _ = workloads.make_inputs(w, seed=0)
-    host = [t.pin_memory() for t in (q_h, k_h, v_h, dO_h)]
-    q, k, v, dO = (t.to(dev) for t in host)
+    w = workloads.get(args.workload)
+    q_h, k_h, v_h, dO_h, m_h = workloads.make_inputs(w, seed=0)
+    host = [t.pin_memory() for t in (q_h, k_h, v_h, dO_h)] + ([m_h.pin_memory()] if m_h is not None else [])
+    q, k, v, dO = (t.to(dev) for t in host[:4])
+    mask = host[4].to(dev) if m_h is not None else None
     scale = w.scale
     stream = torch.cuda.current_stream()
     o = torch.empty(w.B, w.Hq, w.L, w.Ev, dtype=q.dtype, device=dev)
     lse = torch.empty(w.B, w.Hq, w.L, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     bws = torch.empty(max(16, sdpa.backward_workspace_bytes(q, k, v)), dtype=torch.uint8, device=dev)
+    fwd_tc = w.dtype == "bf16" and w.E in (64, 128) and w.Ev in (64, 128)
+    bwd_tc = w.dtype == "bf16" and w.E == w.Ev and w.E in (64, 128)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def fwd():
-        sdpa.sdpa_forward(q, k, v, None, scale, w.is_causal, w.enable_gqa, out=o, lse=lse)
+        sdpa.sdpa_forward(q, k, v, mask, scale, w.is_causal, w.enable_gqa, out=o, lse=lse)
 
     def bwd():
-        sdpa.sdpa_backward(q, k, v, o, dO, lse, None, scale, w.is_causal, w.enable_gqa, dq=dq, dk=dk, dv=dv,
+        sdpa.sdpa_backward(q, k, v, o, dO, lse, mask, scale, w.is_causal, w.enable_gqa, dq=dq, dk=dk, dv=dv,
                            workspace=bws)
 
     if args.phase == "decode":
@@ -272,8 +278,10 @@ def run_ours(args, ws, rank, local):
         h2d = sum(t.numel() * t.element_size() for t in host)
         d2h = sum(t.numel() * t.element_size() for t in out_h)
 
+        dev_in = (q, k, v, dO) + ((mask,) if mask is not None else ())
+
         def e2e_step():
-            for src, dst in zip(host, (q, k, v, dO)):
+            for src, dst in zip(host, dev_in):
                 dst.copy_(src, non_blocking=True)
             fwd()
             bwd()
@@ -297,25 +305,32 @@ def run_ours(args, ws, rank, local):
                "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # ---------------------------------------------------------- launches and roofline
-    bwd_tc = sdpa.backward_workspace_bytes(q, k, v) > 4 * w.B * w.Hq * w.L + 256
-    bwd_launches = 3
+    bwd_launches = 3   # tensor cores: row stats, main, dQ convert; CUDA cores: pre-pass, dQ, dK/dV
     fwd_launches = 1
     launches = args.steps * (fwd_launches + bwd_launches)
     phases = {
         "fwd": {"ms": round(t_fwd, 4), "tflops": round(f_fwd / (t_fwd * 1e-3) / 1e12, 2),
                 "frac_of_bf16_peak": round(f_fwd / (t_fwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                "kernel": "fwd_tc_kernel", "launches_per_step": fwd_launches},
+                "kernel": "fwd_tc_kernel" if fwd_tc else "fwd_simt_kernel", "launches_per_step": fwd_launches},
         "bwd": {"ms": round(t_bwd, 4), "tflops": round(f_bwd / (t_bwd * 1e-3) / 1e12, 2),
                 "frac_of_bf16_peak": round(f_bwd / (t_bwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                 "kernel": "bwd_tc_kernel" if bwd_tc else "bwd_dq_simt_kernel+bwd_dkdv_simt_kernel",
                 "launches_per_step": bwd_launches},
     }
-    if t_fwd >= t_bwd:
+    if t_fwd >= t_bwd and not fwd_tc:
+        achieved = f_fwd / (t_fwd * 1e-3) / 1e12
+        pk = fp32_alu_peak_tflops(sms, peaks["sm_max_mhz"])
+        roof = {"kernel": "fwd_simt_kernel", "bound": "alu", "achieved": round(achieved, 2), "peak": round(pk, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / pk, 4), "traffic": None,
+                "peak_source": f"FFMA: {sms} SMs x 128 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                "algorithmic_per_launch": f_fwd}
+    elif t_fwd >= t_bwd:
         achieved = f_fwd / (t_fwd * 1e-3) / 1e12
         roof = {"kernel": "fwd_tc_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": traffic_for("fwd_tc_kernel", ["fwd_tc.cu", "ptx.cuh", "common.cuh"]),
+                "traffic": (traffic_for("fwd_tc_kernel", ["fwd_tc.cu", "ptx.cuh", "common.cuh"])
+                            if w.name == MAIN else None),
                 "peak_source": f"{peak_src} bf16 dense burst",
                 "algorithmic_per_launch": f_fwd}
     else:
@@ -324,7 +339,8 @@ def run_ours(args, ws, rank, local):
             roof = {"kernel": "bwd_tc_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": round(achieved / peaks["bf16_tflops"], 4),
-                    "traffic": traffic_for("bwd_tc_kernel", ["bwd_tc.cu", "ptx.cuh", "common.cuh"]),
+                    "traffic": (traffic_for("bwd_tc_kernel", ["bwd_tc.cu", "ptx.cuh", "common.cuh"])
+                                if w.name == MAIN else None),
                     "peak_source": f"{peak_src} bf16 dense burst", "algorithmic_per_launch": f_bwd}
         else:
             pk = fp32_alu_peak_tflops(sms, peaks["sm_max_mhz"])
@@ -388,9 +404,10 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step_max, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": MAIN, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "S": w.S, "E": w.E,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "S": w.S, "E": w.E,
                    "Ev": w.Ev, "causal": w.is_causal, "gqa": w.enable_gqa, "scale": w.scale,
+                   "mask": w.mask,
                    "step": "forward (O, LSE) + backward (dQ, dK, dV)", "seed": 0,
                    "l2": "256 MiB flush between timed steps, outside the events",
                    "parallelism": f"replicas x{ws} (no exchange)"},
@@ -461,7 +478,7 @@ def cpu_oracle_sample(w, seconds_target=15.0, steps=None):
     t = statistics.median(times)
     return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"{MAIN}: batch 0, query head 0 (1 of {w.B * w.Hq} heads), forward+backward, "
+            "sample": f"{w.name}: batch 0, query head 0 (1 of {w.B * w.Hq} heads), forward+backward, "
                       f"float64 NumPy, median of {n} runs of {t:.2f} s; BLAS default threads",
             "seconds_per_sample": round(t, 3)}
 

@@ -1,4 +1,4 @@
-// bwd_tc.cu - bf16 backward on the 5th-generation tensor cores (E = Ev = 128).
+// bwd_tc.cu - bf16 backward on the 5th-generation tensor cores (E = Ev = 64 or 128).
 //
 // The hand-derived backward of the course chapter "Scaled dot-product
 // attention (forward and backward)", section 2.3:
@@ -57,7 +57,6 @@ namespace {
 
 using namespace sdpa_ptx;
 
-constexpr int E = 128, Ev = 128;
 constexpr int BKV = 128;       // keys per CTA
 constexpr int BQ = 64;         // queries per iteration
 constexpr int kThreads = 512;
@@ -70,17 +69,26 @@ static_assert(128 * (2 * kRegsElem + kRegsDrain + kRegsOther) <= kThreads * kReg
 static_assert(2 * kRegsElem + kRegsDrain + kRegsOther <= 512, "per sub-partition register file exceeded");
 constexpr int kHalf = BQ / 2;   // query columns per elementwise warp
 
-// shared memory map (bytes; every operand block 1024-aligned)
-constexpr int kKBytes = 2 * BKV * 128;                 // K tile: 2 chunks of [128 keys x 64 dims]
-constexpr int kQTile = 2 * BQ * 128;                   // Q (or dO) tile: 2 chunks of [64 rows x 64 dims]
-constexpr int kStage = 2 * kQTile + 1024;              // Q, dO, rowstats (512 B, padded)
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKBytes;
-constexpr int kOffStage = kOffV + kKBytes;
-constexpr int kOffDS = kOffStage + kNSQ * kStage;      // dS^T [128 keys x 64 queries] bf16 (B operand of dQ^T)
-constexpr int kOffDQ = kOffDS + BKV * 128;             // dQ staging [64 queries x 128 dims] fp32
-constexpr int kOffBar = kOffDQ + BQ * E * 4;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+// Shared memory map for head width E = Ev (bytes; every operand block 1024-aligned).
+// The dQ^T MMA always runs with M = 128: at E = 64 its A rows 64..127 read the
+// 64-dim block after K (the start of V), and the drain never reads those rows of
+// dQ^T, so they cannot reach the result.
+template <int E_>
+struct BwdCfg {
+  static constexpr int E = E_, Ev = E_;
+  static constexpr int ECH = E / 64;                          // 64-element column blocks
+  static constexpr int kKBytes = ECH * BKV * 128;             // K tile: ECH blocks of [128 keys x 64 dims]
+  static constexpr int kQTile = ECH * BQ * 128;               // Q (or dO) tile: ECH blocks of [64 rows x 64 dims]
+  static constexpr int kStage = 2 * kQTile + 1024;            // Q, dO, rowstats (512 B, padded)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKBytes;
+  static constexpr int kOffStage = kOffV + kKBytes;
+  static constexpr int kOffDS = kOffStage + kNSQ * kStage;    // dS^T [128 keys x 64 queries] bf16
+  static constexpr int kOffDQ = kOffDS + BKV * 128;           // dQ staging [64 queries x E] fp32
+  static constexpr int kOffBar = kOffDQ + BQ * E * 4;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static_assert(E == 64 || E == 128, "head width");
+};
 
 // TMEM columns
 constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 320, kColDQ = 384, kColP = 448, kColDS = 480;
@@ -109,6 +117,7 @@ struct TcBwdArgs {
   int Lpad;
 };
 
+template <int E>
 __global__ void __launch_bounds__(256) bwd_rowstats_kernel(TcBwdArgs a) {
   const BwdParams& p = a.p;
   const long long rows = static_cast<long long>(p.B) * p.Hq * a.Lpad;
@@ -120,22 +129,23 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(TcBwdArgs a) {
   float nl = kNegInf, nd = 0.f;
   if (q < p.L) {
     const size_t row = static_cast<size_t>(bh) * p.L + q;
-    const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o) + row * Ev;
-    const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(p.dO) + row * Ev;
-    const __nv_bfloat162 a2 = reinterpret_cast<const __nv_bfloat162*>(o)[lane * 2];
-    const __nv_bfloat162 b2 = reinterpret_cast<const __nv_bfloat162*>(o)[lane * 2 + 1];
-    const __nv_bfloat162 c2 = reinterpret_cast<const __nv_bfloat162*>(dO)[lane * 2];
-    const __nv_bfloat162 d2 = reinterpret_cast<const __nv_bfloat162*>(dO)[lane * 2 + 1];
-    float s = __low2float(a2) * __low2float(c2);
-    s = fmaf(__high2float(a2), __high2float(c2), s);
-    s = fmaf(__low2float(b2), __low2float(d2), s);
-    s = fmaf(__high2float(b2), __high2float(d2), s);
+    const __nv_bfloat162* o =
+        reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(p.o) + row * E);
+    const __nv_bfloat162* dO =
+        reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(p.dO) + row * E);
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < E / 64; ++u) {   // this lane's E/32 elements, as E/64 bf16 pairs
+      const __nv_bfloat162 a2 = o[lane * (E / 64) + u], c2 = dO[lane * (E / 64) + u];
+      s = fmaf(__low2float(a2), __low2float(c2), s);
+      s = fmaf(__high2float(a2), __high2float(c2), s);
+    }
     s = warp_sum(s);
     const float lse = p.lse[row];
     nl = lse == kNegInf ? kNegInf : -lse * kLog2e;
     nd = -s;
     float4* acc = reinterpret_cast<float4*>(p.dq_acc + row * E);
-    acc[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < E / 4) acc[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (lane == 0) {
     float* tile = const_cast<float*>(a.rowstats) + (gr - (q & (BQ - 1))) * 2;   // this row's 64-row tile
@@ -144,6 +154,7 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(TcBwdArgs a) {
   }
 }
 
+template <int E>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p) {
   const float sc = p.scale;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;
@@ -160,9 +171,15 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p) {
   }
 }
 
+template <int E_>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO, TcBwdArgs a) {
+  using C = BwdCfg<E_>;
+  constexpr int E = C::E, Ev = C::Ev, ECH = C::ECH;
+  constexpr int kKBytes = C::kKBytes, kQTile = C::kQTile, kStage = C::kStage;
+  constexpr int kOffK = C::kOffK, kOffV = C::kOffV, kOffStage = C::kOffStage, kOffDS = C::kOffDS,
+                kOffDQ = C::kOffDQ, kOffBar = C::kOffBar;
   const BwdParams& p = a.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -240,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmdO);
       mbar_arrive_expect_tx(kv_full, 2 * kKBytes);
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < ECH; ++c) {
         tma_load_3d(smem + kOffK + c * BKV * 128, &tmK, kv_full, c * 64, k0, bkv);
         tma_load_3d(smem + kOffV + c * BKV * 128, &tmV, kv_full, c * 64, k0, bkv);
       }
@@ -252,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&q_empty[s], ((i / kNSQ) & 1) ^ 1, abort_flag, p.status, status_code(0x31));
         uint8_t* st = smem + kOffStage + s * kStage;
         mbar_arrive_expect_tx(&q_full[s], 2 * kQTile + BQ * 8);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < ECH; ++c) {
           tma_load_3d(st + c * BQ * 128, &tmQ, &q_full[s], c * 64, qt * BQ, bh);
           tma_load_3d(st + kQTile + c * BQ * 128, &tmdO, &q_full[s], c * 64, qt * BQ, bh);
         }
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- MMA issuers
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T: K-major x K-major
       constexpr uint32_t id_kv = idesc_bf16(BKV, E, 0, 1);     // dV, dK: TMEM (K-major) x MN-major
-      constexpr uint32_t id_q = idesc_bf16(E, BQ, 1, 1);       // dQ^T: MN-major x MN-major
+      constexpr uint32_t id_q = idesc_bf16(128, BQ, 1, 1);     // dQ^T: MN-major x MN-major (M = 128 >= E)
       // Operand descriptors, built once; a K-step or a stage moves only the start address.
       const uint32_t stage0 = smem_u32(smem + kOffStage);
       const SmemDesc dK_k = smem_desc(smem_u32(smem + kOffK), 16, 1024);            // K [keys x dims], K-major
@@ -444,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sc2 = m == 0 ? p.scale : 1.f;
       __nv_bfloat16* dst = m == 0 ? dkrow : dvrow;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < E / 32; ++c) {
         uint32_t v[32];
         if (n > 0) {
           tmem_ld32(tmem + lane_off + col + c * 32, v);
@@ -488,10 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the previous bulk reduction must have finished reading the staging rows
       if (e == 0) bulk_wait_read_all();
       named_bar(1, 128);
+      if (e < E) {   // dQ^T lanes past E are padding of the M = 128 MMA
 #pragma unroll
-      for (int j = 0; j < 32; ++j) stage_dq[j * E + e] = __uint_as_float(v0[j]);
+        for (int j = 0; j < 32; ++j) stage_dq[j * E + e] = __uint_as_float(v0[j]);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) stage_dq[(32 + j) * E + e] = __uint_as_float(v1[j]);
+        for (int j = 0; j < 32; ++j) stage_dq[(32 + j) * E + e] = __uint_as_float(v1[j]);
+      }
       fence_proxy_async_smem();
       named_bar(1, 128);
       if (e == 0) {
@@ -511,42 +530,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-bool bwd_tc_supported(int E_, int Ev_) { return E_ == E && Ev_ == Ev; }
-
-int bwd_tc_row_pad() { return BQ; }
-
-cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st) {
+template <int E>
+cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
+  using C = BwdCfg<E>;
   TcBwdArgs a;
   a.p = p;
   a.Lpad = (p.L + BQ - 1) / BQ * BQ;
   a.rowstats = p.D;
+  auto kern = bwd_tc_kernel<E>;
   // The register split in the main kernel assumes the launch reserves exactly kRegsLaunch per thread.
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, bwd_tc_kernel);
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const long long srows = static_cast<long long>(p.B) * p.Hq * a.Lpad;
-  bwd_rowstats_kernel<<<static_cast<unsigned>((srows + 7) / 8), 256, 0, st>>>(a);
+  bwd_rowstats_kernel<E><<<static_cast<unsigned>((srows + 7) / 8), 256, 0, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap tmK, tmV, tmQ, tmdO;
   if (!encode_tmap_bf16_3d(&tmK, p.k, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
-      !encode_tmap_bf16_3d(&tmV, p.v, Ev, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
+      !encode_tmap_bf16_3d(&tmV, p.v, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
       !encode_tmap_bf16_3d(&tmQ, p.q, E, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BQ) ||
-      !encode_tmap_bf16_3d(&tmdO, p.dO, Ev, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BQ))
+      !encode_tmap_bf16_3d(&tmdO, p.dO, E, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BQ))
     return cudaErrorInvalidValue;
-  if ((e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
-      cudaSuccess)
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) != cudaSuccess)
     return e;
   dim3 grid(p.B * p.Hkv, (p.S + BKV - 1) / BKV);
-  bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmK, tmV, tmQ, tmdO, a);
+  kern<<<grid, kThreads, C::kSmemBytes, st>>>(tmK, tmV, tmQ, tmdO, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;
   const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n8 + 255) / 256, 152 * 16));
-  bwd_dq_convert_kernel<<<blocks, 256, 0, st>>>(p);
+  bwd_dq_convert_kernel<E><<<blocks, 256, 0, st>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int E_, int Ev_) { return E_ == Ev_ && (E_ == 64 || E_ == 128); }
+
+int bwd_tc_row_pad() { return BQ; }
+
+cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st) {
+  return p.E == 64 ? run_bwd<64>(p, st) : run_bwd<128>(p, st);
 }
 
 }  // namespace sdpa_impl
