@@ -200,8 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bkv = blockIdx.x, b = bkv / p.Hkv, hkv = bkv - b * p.Hkv;
-  const int k0 = blockIdx.y * BKV;                       // heaviest (causal) tiles first
+  // Causal: grid (KV groups, key tiles), so the heaviest key tiles of every group
+  // start first.  Otherwise every CTA has the same work and the grid is (key
+  // tiles, KV groups): the key-tile CTAs of one group run side by side and share
+  // its Q/dO tiles and dQ accumulator rows in L2.
+  const int bkv = p.causal ? blockIdx.x : blockIdx.y, b = bkv / p.Hkv, hkv = bkv - b * p.Hkv;
+  const int k0 = (p.causal ? blockIdx.y : blockIdx.x) * BKV;
   const int nqt = (p.L + BQ - 1) / BQ;
   const int qt_begin = p.causal ? min(k0 / BQ, nqt) : 0;
   const int per_head = nqt - qt_begin;
@@ -361,12 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* rs = reinterpret_cast<const float*>(smem + kOffStage + s * kStage + 2 * kQTile);
       const int qc = q0 + hf * kHalf;          // first query of this warp's columns
       mbar_wait(&q_full[s], (i / kNSQ) & 1, abort_flag, p.status, status_code(0x38));
-      // this warp's 32 values -lse*log2e, read before the scores arrive
+      // this warp's 32 values -lse*log2e (plus mask*log2e for its key), read before
+      // the scores arrive so the loads' latency overlaps the wait
       float nl[kHalf];
 #pragma unroll
       for (int c = 0; c < kHalf / 4; ++c) {
         const float4 v4 = reinterpret_cast<const float4*>(rs + hf * kHalf)[c];
         nl[4 * c] = v4.x, nl[4 * c + 1] = v4.y, nl[4 * c + 2] = v4.z, nl[4 * c + 3] = v4.w;
+      }
+      if (p.mask) {
+        if (key < p.S) {   // lanes are consecutive keys: each load instruction reads 128 contiguous bytes
+          const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(qc) * p.S + key;
+#pragma unroll
+          for (int j = 0; j < kHalf; ++j)
+            if (qc + j < p.L) nl[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, nl[j]);
+        }
       }
       mbar_wait(s_full, i & 1, abort_flag, p.status, status_code(0x39));
       tc_fence_after();
@@ -380,17 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
-      // t = s alpha log2e - lse log2e
+      // t = s alpha log2e + mask log2e - lse log2e
 #pragma unroll
       for (int j = 0; j < kHalf; j += 2) fma2(x[j], x[j + 1], x[j], x[j + 1], sc, sc, nl[j], nl[j + 1]);
-      if (p.mask) {
-        if (key < p.S) {
-          const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(qc) * p.S + key;
-#pragma unroll
-          for (int j = 0; j < kHalf; ++j)
-            if (qc + j < p.L) x[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, x[j]);
-        }
-      }
       // keys past S, and (causal) keys after the query: both tests are warp-uniform to skip
       if (k0 + BKV > p.S || (p.causal && k0 + BKV - 1 > qc)) {
 #pragma unroll
@@ -555,7 +560,8 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
     return cudaErrorInvalidValue;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) != cudaSuccess)
     return e;
-  dim3 grid(p.B * p.Hkv, (p.S + BKV - 1) / BKV);
+  const unsigned groups = static_cast<unsigned>(p.B * p.Hkv), ktiles = static_cast<unsigned>((p.S + BKV - 1) / BKV);
+  const dim3 grid = p.causal ? dim3(groups, ktiles) : dim3(ktiles, groups);
   kern<<<grid, kThreads, C::kSmemBytes, st>>>(tmK, tmV, tmQ, tmdO, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;

@@ -74,7 +74,7 @@ struct FwdCfg {
   static_assert(NS >= 2, "the K/V ring needs two stages");
 };
 
-template <int ECH, int VCH>
+template <int ECH, int VCH, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, FwdParams p) {
@@ -94,8 +94,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Work units: (batch x query head, pair of 128-row query tiles), listed heaviest
-  // first (causal: the last row pairs see the most key tiles).  The CTAs are
+  // Work units: (batch x query head, pair of 128-row query tiles).  Causal: listed
+  // heaviest first (the last row pairs see the most key tiles).  The CTAs are
   // persistent; CTA c takes units c, 2G-1-c, 2G+c, ... of the list (G CTAs),
   // a snake order that evens out the causal work.
   const int BHq = p.B * p.Hq;
@@ -111,8 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto unit_at = [&](int k) {
     Unit u;
-    const int pair = k / BHq;
-    u.bh = k - pair * BHq;
+    // causal: row pairs outer (the last, heaviest pairs of every head first);
+    // otherwise heads outer, so the pairs of one head run side by side and share its K/V in L2
+    const int pair = p.causal ? k / BHq : k % units;
+    u.bh = p.causal ? k - pair * BHq : k / units;
     u.b = u.bh / p.Hq;
     u.h = u.bh - u.b * p.Hq;
     u.bkv = u.b * p.Hkv + u.h / p.G;
@@ -286,42 +288,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nt == 0) continue;
       const int row_first = u.r0 + t * BM;   // first row of this tile
       const int row = row_first + r;
+      // 256-bit mask loads need 32-byte aligned rows: base aligned and S a multiple of 8
+      const bool mask_v8 = (reinterpret_cast<uintptr_t>(p.mask) & 31) == 0 && (p.S & 7) == 0;
       const float* mrow = (p.mask && row < p.L)
                               ? p.mask + u.b * p.mask_sb + u.h * p.mask_sh + static_cast<size_t>(row) * p.S
                               : nullptr;
       float m_run = kNegInf, l_run = 0.f;
       for (int j = 0; j < nt; ++j) {
-        mbar_wait(&s_full[t], sc_cnt & 1, abort_flag, p.status, status_code(0x18));
-        ++sc_cnt;
-        tc_fence_after();
+        const int kb = j * BN;
         float x[BN];
-        {
+        if (MASKED) {   // the TMEM loads below are executed by the whole warp in either branch
+          // mask * log2e for this row's keys, read before the scores land so the
+          // loads' latency overlaps the wait; whole 32-byte sectors when the rows
+          // are 32-byte aligned (S a multiple of 8), else 16-byte or scalar loads.
+          // Rows past L (mrow == nullptr) read nothing.
+          if (mask_v8) {
+            const float* mtile = mrow + kb;
+#pragma unroll
+            for (int c = 0; c < BN / 8; ++c) {
+              const int key = kb + 8 * c;
+              float m8[8];
+              if (mrow && key < p.S) {
+                asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                             : "=f"(m8[0]), "=f"(m8[1]), "=f"(m8[2]), "=f"(m8[3]), "=f"(m8[4]), "=f"(m8[5]),
+                               "=f"(m8[6]), "=f"(m8[7])
+                             : "l"(mtile + 8 * c));
+              } else {
+#pragma unroll
+                for (int u8 = 0; u8 < 8; ++u8) m8[u8] = 0.f;
+              }
+#pragma unroll
+              for (int u8 = 0; u8 < 8; ++u8) x[8 * c + u8] = m8[u8] * kLog2e;
+            }
+          } else if ((p.S & 3) == 0) {
+#pragma unroll
+            for (int c = 0; c < BN / 4; ++c) {
+              const int key = kb + 4 * c;
+              const float4 mv = mrow && key < p.S ? __ldg(reinterpret_cast<const float4*>(mrow + key))
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+              x[4 * c + 0] = mv.x * kLog2e;
+              x[4 * c + 1] = mv.y * kLog2e;
+              x[4 * c + 2] = mv.z * kLog2e;
+              x[4 * c + 3] = mv.w * kLog2e;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN; ++i) x[i] = mrow && kb + i < p.S ? __ldg(mrow + kb + i) * kLog2e : 0.f;
+          }
+          mbar_wait(&s_full[t], sc_cnt & 1, abort_flag, p.status, status_code(0x18));
+          ++sc_cnt;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tS + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+              fma2(x[c * 32 + i], x[c * 32 + i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sc, sc,
+                   x[c * 32 + i], x[c * 32 + i + 1]);
+          }
+        } else {
+          mbar_wait(&s_full[t], sc_cnt & 1, abort_flag, p.status, status_code(0x18));
+          ++sc_cnt;
+          tc_fence_after();
           uint32_t v[BN];
           tmem_ld128(tS, v);
 #pragma unroll
           for (int i = 0; i < BN; i += 2)
             mul2(x[i], x[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sc, sc);
-        }
-        const int kb = j * BN;
-        if (mrow) {
-          if ((p.S & 3) == 0) {
-            // rows start on 16-byte boundaries only when S is a multiple of 4
-#pragma unroll
-            for (int c = 0; c < BN / 4; ++c) {
-              const int key = kb + 4 * c;
-              if (key < p.S) {
-                const float4 mv = __ldg(reinterpret_cast<const float4*>(mrow + key));
-                x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
-                x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
-                x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
-                x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < BN; ++i)
-              if (kb + i < p.S) x[i] = fmaf(__ldg(mrow + kb + i), kLog2e, x[i]);
-          }
         }
         if (kb + BN > p.S) {
 #pragma unroll
@@ -429,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int ECH, int VCH>
+template <int ECH, int VCH, bool MASKED>
 cudaError_t run(const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<ECH, VCH>;
   alignas(64) CUtensorMap tmQ, tmK, tmV;
@@ -437,7 +471,7 @@ cudaError_t run(const FwdParams& p, cudaStream_t st) {
       !encode_tmap_bf16_3d(&tmK, p.k, C::E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BN) ||
       !encode_tmap_bf16_3d(&tmV, p.v, C::Ev, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BN))
     return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<ECH, VCH>;
+  auto kern = fwd_tc_kernel<ECH, VCH, MASKED>;
   // The register split in the kernel assumes the launch reserves exactly kRegsLaunch per thread.
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -454,16 +488,21 @@ cudaError_t run(const FwdParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <bool MASKED>
+cudaError_t launch_widths(const FwdParams& p, cudaStream_t st) {
+  const int ech = p.E / 64, vch = p.Ev / 64;
+  if (ech == 2 && vch == 2) return run<2, 2, MASKED>(p, st);
+  if (ech == 1 && vch == 1) return run<1, 1, MASKED>(p, st);
+  if (ech == 2 && vch == 1) return run<2, 1, MASKED>(p, st);
+  return run<1, 2, MASKED>(p, st);
+}
+
 }  // namespace
 
 bool fwd_tc_supported(int E, int Ev) { return (E == 64 || E == 128) && (Ev == 64 || Ev == 128); }
 
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t st) {
-  const int ech = p.E / 64, vch = p.Ev / 64;
-  if (ech == 2 && vch == 2) return run<2, 2>(p, st);
-  if (ech == 1 && vch == 1) return run<1, 1>(p, st);
-  if (ech == 2 && vch == 1) return run<2, 1>(p, st);
-  return run<1, 2>(p, st);
+  return p.mask ? launch_widths<true>(p, st) : launch_widths<false>(p, st);
 }
 
 }  // namespace sdpa_impl
