@@ -27,11 +27,23 @@ Sources for each step (page title, section):
     attention (forward and backward)", section 2.3;
   * log-sum-exp statistics max + ln(sum exp(s - max)), natural log, fp32
     shape (B, Hq, L): "Attention" (cuDNN), Scaled Dot Product Attention,
-    Returns ("stats").
+    Returns ("stats");
+  * padding by per-batch lengths seq_len_q / seq_len_kv, diagonal alignment
+    (TOP_LEFT: the diagonal starts at the top-left; BOTTOM_RIGHT: at the
+    bottom-right, aligned with the actual lengths) and the diagonal band
+    (right bound: columns beyond row + right_bound masked; left bound: columns
+    at or before row - left_bound masked): "Attention" (cuDNN), Configurable
+    Options (Padding mask, Diagonal masking options) and Scaled Dot Product
+    Attention, Args (seq_len_q, seq_len_kv, diagonal_alignment,
+    diagonal_band_left_bound, diagonal_band_right_bound).
 
 Readings where the pages are silent (every one also listed in the design notes):
   * a fully blocked row has LSE = -inf, O = 0, dQ = 0 and contributes nothing
-    to dK/dV;
+    to dK/dV; padded query rows (i >= seq_len_q[b]) are such rows;
+  * "row" and "column" of the band bounds are measured from the aligned
+    diagonal (row i's diagonal column is i, or i + seq_len_kv - seq_len_q
+    when bottom-right aligned), and the band, the padding, the additive mask
+    and is_causal (top-left j <= i) all apply together;
   * the scale multiplies Q*K^T only, never the mask;
   * only -inf blocks; a finite large negative number is just a number.
 
@@ -46,7 +58,7 @@ import numpy as np
 
 __all__ = [
     "default_scale", "ref_forward", "ref_backward", "ref_forward_rows",
-    "ref_group", "causal_bias",
+    "ref_group", "causal_bias", "band_bias", "Band",
 ]
 
 NEG_INF = -np.inf
@@ -67,6 +79,55 @@ def causal_bias(L: int, S: int) -> np.ndarray:
     i = np.arange(L)[:, None]
     j = np.arange(S)[None, :]
     return np.where(j <= i, 0.0, NEG_INF)
+
+
+class Band:
+    """Padding and diagonal-band options of one call (cuDNN "Attention" page).
+
+    seq_len_q, seq_len_kv: per-batch actual lengths (sequences of B ints) or
+    None for "the full length"; alignment: "top_left" or "bottom_right";
+    right_bound: None or an int >= 0 (0 = causal about the aligned
+    diagonal); left_bound: None or an int >= 1 (a window of left_bound keys
+    ending at the diagonal).
+    """
+
+    def __init__(self, seq_len_q=None, seq_len_kv=None, alignment="top_left", right_bound=None,
+                 left_bound=None):
+        if alignment not in ("top_left", "bottom_right"):
+            raise ValueError("alignment is top_left or bottom_right")
+        if right_bound is not None and right_bound < 0:
+            raise ValueError("right_bound must be >= 0")
+        if left_bound is not None and left_bound < 1:
+            raise ValueError("left_bound must be >= 1")
+        self.seq_len_q = None if seq_len_q is None else [int(x) for x in seq_len_q]
+        self.seq_len_kv = None if seq_len_kv is None else [int(x) for x in seq_len_kv]
+        self.alignment, self.right_bound, self.left_bound = alignment, right_bound, left_bound
+
+    def lengths(self, b, L, S):
+        Lb = L if self.seq_len_q is None else min(max(self.seq_len_q[b], 0), L)
+        Sb = S if self.seq_len_kv is None else min(max(self.seq_len_kv[b], 0), S)
+        return Lb, Sb
+
+
+def band_bias(L: int, S: int, band: "Band", b: int) -> np.ndarray:
+    """0 where key j is visible to query i of batch b, -inf where it is masked.
+
+    Padding: rows i >= seq_len_q[b] and columns j >= seq_len_kv[b] are
+    masked.  The aligned diagonal of row i is column i (top-left) or
+    i + seq_len_kv[b] - seq_len_q[b] (bottom-right).  Right bound r: columns
+    beyond diagonal + r are masked; left bound w: columns at or before
+    diagonal - w are masked.
+    """
+    Lb, Sb = band.lengths(b, L, S)
+    i = np.arange(L)[:, None]
+    j = np.arange(S)[None, :]
+    diag = i + (Sb - Lb if band.alignment == "bottom_right" else 0)
+    visible = (i < Lb) & (j < Sb)
+    if band.right_bound is not None:
+        visible &= j <= diag + band.right_bound
+    if band.left_bound is not None:
+        visible &= j > diag - band.left_bound
+    return np.where(visible, 0.0, NEG_INF)
 
 
 def _masked_softmax(s: np.ndarray, bias: np.ndarray):
@@ -141,12 +202,14 @@ def _check_shapes(q, k, v, mask, enable_gqa):
     return B, Hq, Hkv, L, S, E, v.shape[3]
 
 
-def _head_bias(mask, b, h, L, S, is_causal):
+def _head_bias(mask, b, h, L, S, is_causal, band=None):
     bias = np.zeros((L, S))
     if mask is not None:
         bias = bias + mask[min(b, mask.shape[0] - 1), min(h, mask.shape[1] - 1)]
     if is_causal:
         bias = bias + causal_bias(L, S)
+    if band is not None:
+        bias = bias + band_bias(L, S, band, b)
     return bias
 
 
@@ -164,10 +227,11 @@ def _head_forward(q, k, v, bias, alpha):
 
 
 def ref_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                return_P=False):
-    """O [B,Hq,L,Ev] and LSE [B,Hq,L] of softmax(alpha*Q*K^T + mask + causal)*V.
+                return_P=False, band=None):
+    """O [B,Hq,L,Ev] and LSE [B,Hq,L] of softmax(alpha*Q*K^T + mask + causal + band)*V.
 
-    Query head h reads KV head h // (Hq // Hkv) (repeat_interleave).
+    Query head h reads KV head h // (Hq // Hkv) (repeat_interleave).  band:
+    None or a Band (padding lengths, diagonal alignment and bounds).
     """
     q, k, v, mask = _as64(q), _as64(k), _as64(v), _as64(mask)
     B, Hq, Hkv, L, S, E, Ev = _check_shapes(q, k, v, mask, enable_gqa)
@@ -180,7 +244,7 @@ def ref_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=Fals
         for h in range(Hq):
             kv = h // G
             o, lse, P = _head_forward(q[b, h], k[b, kv], v[b, kv],
-                                      _head_bias(mask, b, h, L, S, is_causal), alpha)
+                                      _head_bias(mask, b, h, L, S, is_causal, band), alpha)
             O[b, h], LSE[b, h] = o, lse
             if return_P:
                 Ps[b, h] = P
@@ -198,7 +262,7 @@ def _head_backward(q, k, v, P, o, dO, alpha):
 
 
 def ref_backward(q, k, v, dO, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                 return_D=False):
+                 return_D=False, band=None):
     """dQ [B,Hq,L,E], dK [B,Hkv,S,E], dV [B,Hkv,S,Ev] of L = sum(O * dO).
 
     dK and dV of a KV head are summed over the Hq/Hkv query heads that read it
@@ -216,7 +280,7 @@ def ref_backward(q, k, v, dO, mask=None, scale=None, is_causal=False, enable_gqa
     for b in range(B):
         for h in range(Hq):
             kv = h // G
-            bias = _head_bias(mask, b, h, L, S, is_causal)
+            bias = _head_bias(mask, b, h, L, S, is_causal, band)
             o, _, P = _head_forward(q[b, h], k[b, kv], v[b, kv], bias, alpha)
             dq, dk, dv, D = _head_backward(q[b, h], k[b, kv], v[b, kv], P, o, dO[b, h], alpha)
             dQ[b, h] = dq
@@ -227,7 +291,7 @@ def ref_backward(q, k, v, dO, mask=None, scale=None, is_causal=False, enable_gqa
 
 
 def ref_forward_rows(q, k, v, b, h, rows, mask=None, scale=None, is_causal=False,
-                     enable_gqa=False):
+                     enable_gqa=False, band=None):
     """O and LSE of selected query rows of one (b, h): for sampled checks of large runs.
 
     Each row is an independent problem (course chapter, section 2.1: every
@@ -248,11 +312,13 @@ def ref_forward_rows(q, k, v, b, h, rows, mask=None, scale=None, is_causal=False
         bias = bias + _as64(m[rows])
     if is_causal:
         bias = bias + causal_bias(L, S)[rows]
+    if band is not None:
+        bias = bias + band_bias(L, S, band, b)[rows]
     P, lse = _masked_softmax(_scores(qh, kh, alpha), bias)
     return P @ vh, lse
 
 
-def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False):
+def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False, band=None):
     """Forward and backward of the G query heads sharing KV head (b, kv).
 
     Returns (O [G,L,Ev], LSE [G,L], dQ [G,L,E], dK [S,E], dV [S,Ev]) for
@@ -270,9 +336,14 @@ def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False):
         mg = mask[mb:mb + 1]
         if mask.shape[1] != 1:
             mg = mg[:, sl]
-    O, LSE = ref_forward(qg, kg, vg, mg, scale, is_causal, enable_gqa=True)
+    bg = None
+    if band is not None:   # the one batch of the group, with its own lengths
+        bg = Band(None if band.seq_len_q is None else [band.seq_len_q[b]],
+                  None if band.seq_len_kv is None else [band.seq_len_kv[b]],
+                  band.alignment, band.right_bound, band.left_bound)
+    O, LSE = ref_forward(qg, kg, vg, mg, scale, is_causal, enable_gqa=True, band=bg)
     out = [O[0], LSE[0]]
     if dO is not None:
-        dQ, dK, dV = ref_backward(qg, kg, vg, dOg, mg, scale, is_causal, enable_gqa=True)
+        dQ, dK, dV = ref_backward(qg, kg, vg, dOg, mg, scale, is_causal, enable_gqa=True, band=bg)
         out += [dQ[0], dK[0, 0], dV[0, 0]]
     return tuple(out)
