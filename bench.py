@@ -55,7 +55,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--workload", default=MAIN,
-                    choices=["tiny_f32", "tiny_f32_causal", "mha_causal_e64", "gqa_causal_e128", "padded_mask_e128"],
+                    choices=["tiny_f32", "tiny_f32_causal", "mha_causal_e64", "gqa_causal_e128", "padded_mask_e128",
+                             "padded_seqlen_e128", "gqa_swa_e128"],
                     help="prefill workload of the step (default: the GQA causal E=128 headline workload)")
     ap.add_argument("--phase", choices=["all", "fwd", "bwd", "decode"], default="all",
                     help="profiling aid: run only the forward loop, the backward loop or the decode leg")
@@ -188,6 +189,27 @@ def traffic_for(kernel: str, sources):
     return None
 
 
+def visible_pairs(w, spec) -> int:
+    """(query, key) pairs a banded workload computes, summed over batches and query heads.
+
+    Row i < Lb of batch b sees keys lo(i)..hi(i) with the padding lengths and band
+    of the sdpa_options contract (cuDNN "Attention": Padding mask, Diagonal masking
+    options); FLOPs are then 4*E (forward) and 10*E (backward) per pair, the same
+    per-pair cost as the nominal formulas.
+    """
+    import numpy as np
+    total = 0
+    for b in range(w.B):
+        Lb = w.L if spec["seq_len_q"] is None else min(spec["seq_len_q"][b], w.L)
+        Sb = w.S if spec["seq_len_kv"] is None else min(spec["seq_len_kv"][b], w.S)
+        i = np.arange(Lb, dtype=np.int64)
+        diag = i + (Sb - Lb if spec["alignment"] == "bottom_right" else 0)
+        hi = np.full(Lb, Sb - 1) if spec["right_bound"] is None else np.minimum(Sb - 1, diag + spec["right_bound"])
+        lo = np.zeros(Lb, np.int64) if spec["left_bound"] is None else np.maximum(0, diag - spec["left_bound"] + 1)
+        total += int(np.maximum(0, hi - lo + 1).sum())
+    return total * w.Hq
+
+
 def fp32_alu_peak_tflops(sms: int, mhz: float) -> float:
     """FFMA peak: SMs x 128 fp32 lanes x 2 flops x clock."""
     return sms * 128 * 2 * mhz * 1e6 / 1e12
@@ -213,6 +235,14 @@ def run_ours(args, ws, rank, local):
     host = [t.pin_memory() for t in (q_h, k_h, v_h, dO_h)] + ([m_h.pin_memory()] if m_h is not None else [])
     q, k, v, dO = (t.to(dev) for t in host[:4])
     mask = host[4].to(dev) if m_h is not None else None
+    spec = workloads.make_band(w, seed=0)
+    band = None
+    if spec is not None:
+        lens = [None if spec[n] is None else torch.tensor(spec[n], dtype=torch.int32).pin_memory()
+                for n in ("seq_len_q", "seq_len_kv")]
+        host += [t for t in lens if t is not None]
+        band = sdpa.Band(*[None if t is None else t.to(dev) for t in lens], spec["alignment"], spec["right_bound"],
+                         spec["left_bound"])
     scale = w.scale
     stream = torch.cuda.current_stream()
     o = torch.empty(w.B, w.Hq, w.L, w.Ev, dtype=q.dtype, device=dev)
@@ -224,11 +254,11 @@ def run_ours(args, ws, rank, local):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def fwd():
-        sdpa.sdpa_forward(q, k, v, mask, scale, w.is_causal, w.enable_gqa, out=o, lse=lse)
+        sdpa.sdpa_forward(q, k, v, mask, scale, w.is_causal, w.enable_gqa, out=o, lse=lse, band=band)
 
     def bwd():
         sdpa.sdpa_backward(q, k, v, o, dO, lse, mask, scale, w.is_causal, w.enable_gqa, dq=dq, dk=dk, dv=dv,
-                           workspace=bws)
+                           workspace=bws, band=band)
 
     if args.phase == "decode":
         return run_decode_only(args, ws, local, dev, peaks)
@@ -265,7 +295,11 @@ def run_ours(args, ws, rank, local):
     t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     t_step = t_fwd + t_bwd
     t_step_max = reduce_max(t_step, ws)
-    f_fwd, f_bwd = w.flops("fwd"), w.flops("bwd")
+    if spec is None:
+        f_fwd, f_bwd = w.flops("fwd"), w.flops("bwd")
+    else:
+        pairs = visible_pairs(w, spec)
+        f_fwd, f_bwd = 4.0 * w.E * pairs, 10.0 * w.E * pairs
     value = ws * (f_fwd + f_bwd) / (t_step_max * 1e-3) / 1e12
     assert sdpa.last_device_status() == 0
 
@@ -278,7 +312,8 @@ def run_ours(args, ws, rank, local):
         h2d = sum(t.numel() * t.element_size() for t in host)
         d2h = sum(t.numel() * t.element_size() for t in out_h)
 
-        dev_in = (q, k, v, dO) + ((mask,) if mask is not None else ())
+        dev_in = (q, k, v, dO) + ((mask,) if mask is not None else ()) + tuple(
+            t for t in ((band.seq_len_q, band.seq_len_kv) if band is not None else ()) if t is not None)
 
         def e2e_step():
             for src, dst in zip(host, dev_in):
@@ -407,7 +442,9 @@ def run_ours(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "S": w.S, "E": w.E,
                    "Ev": w.Ev, "causal": w.is_causal, "gqa": w.enable_gqa, "scale": w.scale,
-                   "mask": w.mask,
+                   "mask": w.mask, "band": spec,
+                   "flops": "visible (query, key) pairs x 4E / 10E" if spec is not None else
+                            "4/10 x B*Hq*L*S*E, halved for causal",
                    "step": "forward (O, LSE) + backward (dQ, dK, dV)", "seed": 0,
                    "l2": "256 MiB flush between timed steps, outside the events",
                    "parallelism": f"replicas x{ws} (no exchange)"},
@@ -454,21 +491,28 @@ def _oracle_head_sample(w, nheads=1):
     ks, vs = k[:1, kv_heads], v[:1, kv_heads]
     ms = None if mask is None else mask[:1]
     sub = w.with_(B=1, Hq=nheads, Hkv=len(kv_heads))
-    flops = sub.flops("fwd") + sub.flops("bwd")
+    spec = workloads.make_band(w, seed=0)
+    if spec is not None:   # batch 0's lengths
+        spec = dict(spec, **{n: None if spec[n] is None else spec[n][:1] for n in ("seq_len_q", "seq_len_kv")})
+        flops = 14.0 * w.E * visible_pairs(sub, spec)
+    else:
+        flops = sub.flops("fwd") + sub.flops("bwd")
     del q, k, v, dO, mask
-    return (qs, ks, vs, dOs, ms), sub, flops, torch
+    return (qs, ks, vs, dOs, ms), sub, flops, spec
 
 
 def cpu_oracle_sample(w, seconds_target=15.0, steps=None):
     import oracle
-    (qs, ks, vs, dOs, ms), sub, flops, _ = _oracle_head_sample(w)
+    (qs, ks, vs, dOs, ms), sub, flops, spec = _oracle_head_sample(w)
+    band = None if spec is None else oracle.Band(spec["seq_len_q"], spec["seq_len_kv"], spec["alignment"],
+                                                 spec["right_bound"], spec["left_bound"])
     times = []
     n = 0
     t_start = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv)
-        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv)
+        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band)
+        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band)
         times.append(time.perf_counter() - t0)
         n += 1
         if steps is not None and n >= steps:

@@ -35,7 +35,9 @@
  *  mask      Additive: -inf blocks a (query, key) pair, finite values are
  *            added to the scaled score.  NULL = no mask.
  *  causal    is_causal != 0 blocks key j for query i when j > i (top-left
- *            aligned, for any L and S).  Combines with a mask.
+ *            aligned, for any L and S).  Combines with a mask.  The *_opts
+ *            entry points take padding lengths, a diagonal alignment and band
+ *            bounds instead (sdpa_options below).
  *  GQA       Query head h reads KV head h / (Hq / Hkv).  Hq != Hkv requires
  *            enable_gqa != 0 and Hq % Hkv == 0.  dk and dv are summed over
  *            the Hq / Hkv query heads that share a KV head.
@@ -84,8 +86,8 @@ typedef struct {
  * lse[b,h,i] = max_j t_ij + ln(sum_j exp(t_ij - max_j t_ij)), t = the masked
  * scaled scores (course chapter sections 2.1-2.2; cuDNN "Attention",
  * Scaled Dot Product Attention, stats).  lse is always written.
- * A bf16 call with L == 1, no causal flag and no mask runs the split-KV decode
- * (same contract as sdpa_decode with num_splits = 0) and needs the workspace
+ * A bf16 call with L == 1 (E, Ev in {64, 128}) runs the split-KV decode (same
+ * contract as sdpa_decode with num_splits = 0) and needs the workspace
  * reported by sdpa_forward_workspace_bytes; every other call needs none
  * (workspace may then be NULL with workspace_bytes = 0). */
 sdpa_status sdpa_forward(const sdpa_shape* shape,
@@ -125,7 +127,9 @@ size_t sdpa_backward_workspace_bytes(const sdpa_shape* shape);
  * o = sum_s exp(lse_s - lse) o_s (cuDNN "Attention": log-sum-exp statistics
  * and their split-KV merges).  num_splits = 0 picks a count from the GPU's SM
  * count.  The result equals the plain forward up to fp32 rounding for every
- * split count.  No causal flag (it would leave one key for L == 1). */
+ * split count.  No causal flag here (top-left causal would leave one key for
+ * L == 1); sdpa_decode_opts takes padding lengths (e.g. each sequence's cache
+ * length) and a bottom-right band. */
 sdpa_status sdpa_decode(const sdpa_shape* shape,
                         const void* q, const void* k, const void* v,
                         const float* mask_or_null, double scale, int enable_gqa,
@@ -172,6 +176,67 @@ sdpa_status sdpa_decode_noalloc(const sdpa_shape* shape,
                                 int num_splits,
                                 void* o, float* lse,
                                 void* stream /* cudaStream_t */);
+
+/* Padding and diagonal-band options of the *_opts entry points (cuDNN
+ * "Attention": Configurable Options, Padding mask and Diagonal masking
+ * options; Scaled Dot Product Attention, Args seq_len_q, seq_len_kv,
+ * diagonal_alignment, diagonal_band_left_bound, diagonal_band_right_bound).
+ *
+ *  seq_len_q, seq_len_kv  NULL, or DEVICE arrays of B int32 (4-byte aligned)
+ *            holding each batch's actual query / key-value length; values are
+ *            clamped to [0, L] and [0, S].  Query rows i >= seq_len_q[b] are
+ *            padding: o = 0, lse = -inf, dq = 0, and they add nothing to dk,
+ *            dv.  Keys j >= seq_len_kv[b] are masked (dk = dv = 0 there).  A
+ *            batch of length 0 is skipped this way.  NULL = full length.
+ *  diagonal_alignment  SDPA_TOP_LEFT: row i's diagonal is column i.
+ *            SDPA_BOTTOM_RIGHT: column i + Skv_b - Sq_b, with the actual
+ *            lengths of batch b (prefix-LM and decode diagonals).
+ *  right_bound  < 0: none.  >= 0: columns beyond diagonal + right_bound are
+ *            masked (0 = causal about the aligned diagonal).
+ *  left_bound   <= 0: none.  >= 1: columns at or before diagonal - left_bound
+ *            are masked (a sliding window of left_bound keys ending at the
+ *            diagonal).
+ * All of it applies together with the additive mask; a row left without keys
+ * follows the empty-row rule above.  The backward must get the forward's
+ * options.  Other values of diagonal_alignment, or misaligned length
+ * pointers, -> INVALID_ARG. */
+typedef enum { SDPA_TOP_LEFT = 0, SDPA_BOTTOM_RIGHT = 1 } sdpa_diag_alignment;
+
+typedef struct {
+  const int32_t* seq_len_q;
+  const int32_t* seq_len_kv;
+  int32_t diagonal_alignment;  /* sdpa_diag_alignment */
+  int32_t right_bound;
+  int32_t left_bound;
+} sdpa_options;
+
+/* sdpa_forward, sdpa_backward and sdpa_decode with sdpa_options in place of
+ * is_causal (is_causal != 0 equals {NULL, NULL, SDPA_TOP_LEFT, 0, 0}).  Same
+ * arguments, workspaces, routing and errors otherwise; options must not be
+ * NULL (INVALID_ARG).  The lengths are read on the device, so the work skipped
+ * for padding is decided by the kernels. */
+sdpa_status sdpa_forward_opts(const sdpa_shape* shape, const sdpa_options* options,
+                              const void* q, const void* k, const void* v,
+                              const float* mask_or_null, double scale, int enable_gqa,
+                              void* o, float* lse,
+                              void* workspace, size_t workspace_bytes,
+                              void* stream /* cudaStream_t */);
+
+sdpa_status sdpa_backward_opts(const sdpa_shape* shape, const sdpa_options* options,
+                               const void* q, const void* k, const void* v,
+                               const void* o, const void* dO, const float* lse,
+                               const float* mask_or_null, double scale, int enable_gqa,
+                               void* dq, void* dk, void* dv,
+                               void* workspace, size_t workspace_bytes,
+                               void* stream /* cudaStream_t */);
+
+sdpa_status sdpa_decode_opts(const sdpa_shape* shape, const sdpa_options* options,
+                             const void* q, const void* k, const void* v,
+                             const float* mask_or_null, double scale, int enable_gqa,
+                             int num_splits,
+                             void* o, float* lse,
+                             void* workspace, size_t workspace_bytes,
+                             void* stream /* cudaStream_t */);
 
 /* Static, NUL-terminated description of a status code. */
 const char* sdpa_status_string(sdpa_status status);

@@ -19,7 +19,7 @@ from .build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "SdpaError", "load_library", "exported_symbols", "sdpa_forward", "sdpa_backward", "sdpa_decode",
     "forward_workspace_bytes", "backward_workspace_bytes", "decode_workspace_bytes",
-    "decode_num_splits", "last_device_status", "Shape", "build", "LIB_PATH",
+    "decode_num_splits", "last_device_status", "Shape", "Options", "Band", "build", "LIB_PATH",
 ]
 
 SDPA_F32, SDPA_BF16 = 0, 1
@@ -29,7 +29,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: 
 EXPORTS = (
     "sdpa_forward", "sdpa_forward_workspace_bytes", "sdpa_backward", "sdpa_backward_workspace_bytes",
     "sdpa_decode", "sdpa_decode_workspace_bytes", "sdpa_decode_num_splits", "sdpa_status_string",
-    "sdpa_last_device_status", "sdpa_decode_noalloc",
+    "sdpa_last_device_status", "sdpa_decode_noalloc", "sdpa_forward_opts", "sdpa_backward_opts",
+    "sdpa_decode_opts",
 )
 
 
@@ -44,6 +45,38 @@ class Shape(ctypes.Structure):
                 ("L", ctypes.c_int64), ("S", ctypes.c_int64), ("E", ctypes.c_int64),
                 ("Ev", ctypes.c_int64), ("dtype", ctypes.c_int32), ("mask_b", ctypes.c_int32),
                 ("mask_h", ctypes.c_int32)]
+
+
+class Options(ctypes.Structure):
+    """sdpa_options: padding lengths (device int32 [B] or NULL), diagonal alignment, band bounds."""
+    _fields_ = [("seq_len_q", ctypes.c_void_p), ("seq_len_kv", ctypes.c_void_p),
+                ("diagonal_alignment", ctypes.c_int32), ("right_bound", ctypes.c_int32),
+                ("left_bound", ctypes.c_int32)]
+
+
+class Band:
+    """Padding and diagonal band of a call (see sdpa_options in include/sdpa.h).
+
+    seq_len_q, seq_len_kv: None or CUDA int32 tensors of B lengths; alignment:
+    "top_left" or "bottom_right"; right_bound: None or >= 0 (0 = causal);
+    left_bound: None or >= 1 (sliding window).
+    """
+
+    def __init__(self, seq_len_q=None, seq_len_kv=None, alignment="top_left", right_bound=None, left_bound=None):
+        self.seq_len_q, self.seq_len_kv = seq_len_q, seq_len_kv
+        self.alignment, self.right_bound, self.left_bound = alignment, right_bound, left_bound
+
+    def options(self) -> Options:
+        import torch
+        for t in (self.seq_len_q, self.seq_len_kv):
+            if t is not None and (not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous()):
+                raise ValueError("seq_len tensors must be contiguous CUDA int32")
+        align = {"top_left": 0, "bottom_right": 1}.get(self.alignment)
+        if align is None:
+            raise ValueError("alignment is top_left or bottom_right")
+        return Options(_ptr(self.seq_len_q), _ptr(self.seq_len_kv), align,
+                       -1 if self.right_bound is None else int(self.right_bound),
+                       0 if self.left_bound is None else int(self.left_bound))
 
 
 _lib = None
@@ -72,6 +105,16 @@ def load_library(path: Optional[str] = None):
     lib.sdpa_decode_noalloc.argtypes = [SP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int, _P, _P,
                                         _P]
     lib.sdpa_decode_noalloc.restype = ctypes.c_int
+    OP = ctypes.POINTER(Options)
+    lib.sdpa_forward_opts.argtypes = [SP, OP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, _P, _P, _P,
+                                      ctypes.c_size_t, _P]
+    lib.sdpa_forward_opts.restype = ctypes.c_int
+    lib.sdpa_backward_opts.argtypes = [SP, OP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int,
+                                       _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.sdpa_backward_opts.restype = ctypes.c_int
+    lib.sdpa_decode_opts.argtypes = [SP, OP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int, _P, _P,
+                                     _P, ctypes.c_size_t, _P]
+    lib.sdpa_decode_opts.restype = ctypes.c_int
     for fn in ("sdpa_forward_workspace_bytes", "sdpa_backward_workspace_bytes"):
         getattr(lib, fn).argtypes = [SP]
         getattr(lib, fn).restype = ctypes.c_size_t
@@ -175,8 +218,12 @@ def decode_num_splits(q, k, v) -> int:
 
 
 def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                 out=None, lse=None, workspace=None, stream=None):
-    """O [B,Hq,L,Ev] (dtype of q) and LSE [B,Hq,L] fp32 of softmax(scale*q k^T + mask) v."""
+                 out=None, lse=None, workspace=None, stream=None, band=None):
+    """O [B,Hq,L,Ev] (dtype of q) and LSE [B,Hq,L] fp32 of softmax(scale*q k^T + mask) v.
+
+    band: None, or a Band (padding lengths, diagonal alignment, bounds) used in
+    place of is_causal (sdpa_forward_opts).
+    """
     import torch
     lib = load_library()
     _check_tensors(q, k, v, mask)
@@ -189,17 +236,24 @@ def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=Fal
     need = int(lib.sdpa_forward_workspace_bytes(ctypes.byref(shp)))
     if workspace is None and need:
         workspace = _workspace(need, q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if band is not None:
+        opts = band.options()
+        st = lib.sdpa_forward_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(mask),
+                                   _scale(scale), int(bool(enable_gqa)), _ptr(out), _ptr(lse), _ptr(workspace), wsb,
+                                   _stream(stream))
+        _raise(st, "sdpa_forward_opts")
+        return out, lse
     st = lib.sdpa_forward(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), _scale(scale),
                           int(bool(is_causal)), int(bool(enable_gqa)), _ptr(out), _ptr(lse), _ptr(workspace),
-                          0 if workspace is None else workspace.numel() * workspace.element_size(),
-                          _stream(stream))
+                          wsb, _stream(stream))
     _raise(st, "sdpa_forward")
     return out, lse
 
 
 def sdpa_backward(q, k, v, o, dO, lse, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                  dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of sum(O * dO); o and lse are the forward's outputs."""
+                  dq=None, dk=None, dv=None, workspace=None, stream=None, band=None):
+    """dQ, dK, dV of sum(O * dO); o and lse are the forward's outputs (same band)."""
     import torch
     lib = load_library()
     _check_tensors(q, k, v, o, dO, lse, mask)
@@ -209,17 +263,24 @@ def sdpa_backward(q, k, v, o, dO, lse, mask=None, scale=None, is_causal=False, e
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
         workspace = _workspace(lib.sdpa_backward_workspace_bytes(ctypes.byref(shp)), q.device)
+    wsb = workspace.numel() * workspace.element_size()
+    if band is not None:
+        opts = band.options()
+        st = lib.sdpa_backward_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(dO), _ptr(lse), _ptr(mask), _scale(scale), int(bool(enable_gqa)), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(workspace), wsb, _stream(stream))
+        _raise(st, "sdpa_backward_opts")
+        return dq, dk, dv
     st = lib.sdpa_backward(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
                            _ptr(mask), _scale(scale), int(bool(is_causal)), int(bool(enable_gqa)), _ptr(dq),
-                           _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                           _stream(stream))
+                           _ptr(dk), _ptr(dv), _ptr(workspace), wsb, _stream(stream))
     _raise(st, "sdpa_backward")
     return dq, dk, dv
 
 
 def sdpa_decode(q, k, v, mask=None, scale=None, enable_gqa=False, num_splits=0,
-                out=None, lse=None, workspace=None, stream=None):
-    """Split-KV decode forward (bf16): same outputs as sdpa_forward."""
+                out=None, lse=None, workspace=None, stream=None, band=None):
+    """Split-KV decode forward (bf16): same outputs as sdpa_forward (band: sdpa_decode_opts)."""
     import torch
     lib = load_library()
     _check_tensors(q, k, v, mask)
@@ -231,9 +292,17 @@ def sdpa_decode(q, k, v, mask=None, scale=None, enable_gqa=False, num_splits=0,
         lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = _workspace(lib.sdpa_decode_workspace_bytes(ctypes.byref(shp), int(num_splits)), q.device)
+    wsb = workspace.numel() * workspace.element_size()
+    if band is not None:
+        opts = band.options()
+        st = lib.sdpa_decode_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(mask),
+                                  _scale(scale), int(bool(enable_gqa)), int(num_splits), _ptr(out), _ptr(lse),
+                                  _ptr(workspace), wsb, _stream(stream))
+        _raise(st, "sdpa_decode_opts")
+        return out, lse
     st = lib.sdpa_decode(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), _scale(scale),
-                         int(bool(enable_gqa)), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(stream))
+                         int(bool(enable_gqa)), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace), wsb,
+                         _stream(stream))
     _raise(st, "sdpa_decode")
     return out, lse
 

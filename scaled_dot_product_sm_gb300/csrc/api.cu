@@ -101,8 +101,29 @@ sdpa_status check_scale(double scale, int E, float* alpha) {
 
 sdpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
 
+// The band of the plain entry points: no padding, top-left, causal = right bound 0.
+Band plain_band(int is_causal) { return Band{nullptr, nullptr, 0, is_causal ? 0 : -1, 0}; }
+
+// Checks sdpa_options and turns them into a Band (NULL options = no padding, no band).
+sdpa_status band_from_options(const sdpa_options* o, const Checked& c, Band* band) {
+  *band = plain_band(0);
+  if (!o) return SDPA_OK;
+  if (o->diagonal_alignment != SDPA_TOP_LEFT && o->diagonal_alignment != SDPA_BOTTOM_RIGHT)
+    return SDPA_ERR_INVALID_ARG;
+  if ((o->seq_len_q && (reinterpret_cast<uintptr_t>(o->seq_len_q) & 3)) ||
+      (o->seq_len_kv && (reinterpret_cast<uintptr_t>(o->seq_len_kv) & 3)))
+    return SDPA_ERR_INVALID_ARG;
+  const long long cap = static_cast<long long>(c.L) + c.S;   // a bound this wide no longer restricts
+  band->seqlen_q = o->seq_len_q;
+  band->seqlen_kv = o->seq_len_kv;
+  band->bottom_right = o->diagonal_alignment == SDPA_BOTTOM_RIGHT ? 1 : 0;
+  band->right = o->right_bound < 0 ? -1 : static_cast<int>(std::min<long long>(o->right_bound, cap));
+  band->left = o->left_bound <= 0 ? 0 : static_cast<int>(std::min<long long>(o->left_bound, cap));
+  return SDPA_OK;
+}
+
 void fill_fwd(FwdParams& p, const Checked& c, const void* q, const void* k, const void* v, const float* mask,
-              float alpha, int causal, void* o, float* lse) {
+              float alpha, const Band& band, void* o, float* lse) {
   p.q = q;
   p.k = k;
   p.v = v;
@@ -121,7 +142,7 @@ void fill_fwd(FwdParams& p, const Checked& c, const void* q, const void* k, cons
   p.mask_sh = c.mask_sh;
   p.scale = alpha;
   p.scale_log2 = alpha * kLog2e;
-  p.causal = causal ? 1 : 0;
+  p.band = band;
   p.status = status_ptr();
 }
 
@@ -165,10 +186,7 @@ size_t decode_ws(const Checked& c, int nsplit) {
   return round_up(rows * nsplit * c.Ev * sizeof(float), 256) + round_up(rows * nsplit * sizeof(float), 256);
 }
 
-bool routes_to_decode(const Checked& c, bool has_mask, int causal) {
-  (void)has_mask;
-  return c.bf16 && c.L == 1 && !causal && decode_supported(c.E, c.Ev);
-}
+bool routes_to_decode(const Checked& c) { return c.bf16 && c.L == 1 && decode_supported(c.E, c.Ev); }
 
 bool bwd_uses_tc(const Checked& c) { return c.bf16 && bwd_tc_supported(c.E, c.Ev); }
 
@@ -188,9 +206,9 @@ size_t bwd_ws(const Checked& c) {
   return bytes;
 }
 
-sdpa_status run_decode(const Checked& c, const void* q, const void* k, const void* v, const float* mask,
-                       float alpha, int num_splits, void* o, float* lse, void* ws, size_t ws_bytes,
-                       cudaStream_t st) {
+sdpa_status run_decode(const Checked& c, const Band& band, const void* q, const void* k, const void* v,
+                       const float* mask, float alpha, int num_splits, void* o, float* lse, void* ws,
+                       size_t ws_bytes, cudaStream_t st) {
   int nsplit, kps;
   split_layout(c, num_splits > 0 ? num_splits : auto_splits(c), &nsplit, &kps);
   if (c.B * c.Hkv * ((c.G * c.L + decode_rows_per_cta() - 1) / decode_rows_per_cta()) > 65535)
@@ -198,7 +216,7 @@ sdpa_status run_decode(const Checked& c, const void* q, const void* k, const voi
   const size_t need = decode_ws(c, nsplit);
   if (!ws || ws_bytes < need || !aligned16(ws)) return SDPA_ERR_INVALID_ARG;
   DecodeParams dp;
-  fill_fwd(dp.f, c, q, k, v, mask, alpha, 0, o, lse);
+  fill_fwd(dp.f, c, q, k, v, mask, alpha, band, o, lse);
   const size_t rows = static_cast<size_t>(c.B) * c.Hq * c.L;
   dp.part_o = static_cast<float*>(ws);
   dp.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
@@ -252,25 +270,34 @@ bool encode_tmap_bf16_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1,
 
 using namespace sdpa_impl;
 
-extern "C" {
+namespace sdpa_impl {
+namespace {
 
-sdpa_status sdpa_forward(const sdpa_shape* shape, const void* q, const void* k, const void* v,
-                         const float* mask_or_null, double scale, int is_causal, int enable_gqa, void* o,
+sdpa_status check_io(const Checked& c, const void* q, const void* k, const void* v, const float* mask, void* o,
+                     float* lse) {
+  (void)c;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (mask && !aligned16(mask)))
+    return SDPA_ERR_INVALID_ARG;
+  return SDPA_OK;
+}
+
+sdpa_status forward_impl(const sdpa_shape* shape, const sdpa_options* opts, int is_causal, const void* q,
+                         const void* k, const void* v, const float* mask, double scale, int enable_gqa, void* o,
                          float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   Checked c;
-  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
+  sdpa_status s = check_shape(shape, enable_gqa, mask != nullptr, &c);
   if (s != SDPA_OK) return s;
   float alpha;
   if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
-  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      (mask_or_null && !aligned16(mask_or_null)))
-    return SDPA_ERR_INVALID_ARG;
+  if ((s = check_io(c, q, k, v, mask, o, lse)) != SDPA_OK) return s;
+  Band band = plain_band(is_causal);
+  if (opts && (s = band_from_options(opts, c, &band)) != SDPA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (routes_to_decode(c, mask_or_null != nullptr, is_causal))
-    return run_decode(c, q, k, v, mask_or_null, alpha, 0, o, lse, workspace, workspace_bytes, st);
+  if (routes_to_decode(c)) return run_decode(c, band, q, k, v, mask, alpha, 0, o, lse, workspace, workspace_bytes, st);
   FwdParams p;
-  fill_fwd(p, c, q, k, v, mask_or_null, alpha, is_causal, o, lse);
+  fill_fwd(p, c, q, k, v, mask, alpha, band, o, lse);
   if (c.bf16 && fwd_tc_supported(c.E, c.Ev)) {
     if ((c.L + 255) / 256 > 65535) return SDPA_ERR_UNSUPPORTED;
     return from_cuda(launch_fwd_tc(p, st));
@@ -279,10 +306,113 @@ sdpa_status sdpa_forward(const sdpa_shape* shape, const void* q, const void* k, 
   return from_cuda(launch_fwd_simt(p, c.bf16 ? 1 : 0, st));
 }
 
+sdpa_status decode_impl(const sdpa_shape* shape, const sdpa_options* opts, const void* q, const void* k,
+                        const void* v, const float* mask, double scale, int enable_gqa, int num_splits, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, bool static_scratch, void* stream) {
+  Checked c;
+  sdpa_status s = check_shape(shape, enable_gqa, mask != nullptr, &c);
+  if (s != SDPA_OK) return s;
+  float alpha;
+  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
+  if (num_splits < 0) return SDPA_ERR_INVALID_ARG;
+  if ((s = check_io(c, q, k, v, mask, o, lse)) != SDPA_OK) return s;
+  Band band = plain_band(0);
+  if (opts && (s = band_from_options(opts, c, &band)) != SDPA_OK) return s;
+  if (!c.bf16 || !decode_supported(c.E, c.Ev)) return SDPA_ERR_UNSUPPORTED;
+  const int want = num_splits > 0 ? num_splits : auto_splits(c);
+  if (static_scratch) {
+    int nsplit, kps;
+    split_layout(c, want, &nsplit, &kps);
+    if (decode_ws(c, nsplit) > SDPA_DECODE_STATIC_SCRATCH_BYTES) return SDPA_ERR_UNSUPPORTED;
+    size_t cap = 0;
+    if (decode_static_scratch(&workspace, &cap) != cudaSuccess) return SDPA_ERR_CUDA;
+    workspace_bytes = cap;
+  }
+  return run_decode(c, band, q, k, v, mask, alpha, want, o, lse, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+sdpa_status backward_impl(const sdpa_shape* shape, const sdpa_options* opts, int is_causal, const void* q,
+                          const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                          const float* mask, double scale, int enable_gqa, void* dq, void* dk, void* dv,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  Checked c;
+  sdpa_status s = check_shape(shape, enable_gqa, mask != nullptr, &c);
+  if (s != SDPA_OK) return s;
+  float alpha;
+  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return SDPA_ERR_INVALID_ARG;
+  if (mask && !aligned16(mask)) return SDPA_ERR_INVALID_ARG;
+  Band band = plain_band(is_causal);
+  if (opts && (s = band_from_options(opts, c, &band)) != SDPA_OK) return s;
+  const size_t need = bwd_ws(c);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SDPA_ERR_INVALID_ARG;
+  BwdParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dO = dO;
+  p.lse = lse;
+  p.mask = mask;
+  p.D = static_cast<float*>(workspace);
+  p.dq_acc = bwd_uses_tc(c) ? reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_stats_bytes(c))
+                            : nullptr;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = c.B;
+  p.Hq = c.Hq;
+  p.Hkv = c.Hkv;
+  p.L = c.L;
+  p.S = c.S;
+  p.E = c.E;
+  p.Ev = c.Ev;
+  p.G = c.G;
+  p.mask_sb = c.mask_sb;
+  p.mask_sh = c.mask_sh;
+  p.scale = alpha;
+  p.scale_log2 = alpha * kLog2e;
+  p.band = band;
+  p.status = status_ptr();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.dq_acc) {
+    if (c.B * c.Hkv > 65535 * 64 || (c.S + 127) / 128 > 65535) return SDPA_ERR_UNSUPPORTED;
+    return from_cuda(launch_bwd_tc(p, st));
+  }
+  cudaError_t e = launch_bwd_preprocess(p, c.bf16 ? 1 : 0, st);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  if ((c.L + 15) / 16 > 65535 || (c.S + 15) / 16 > 65535 || static_cast<long long>(c.B) * c.Hq > 65535)
+    return SDPA_ERR_UNSUPPORTED;
+  return from_cuda(launch_bwd_simt(p, c.bf16 ? 1 : 0, st));
+}
+
+}  // namespace
+}  // namespace sdpa_impl
+
+extern "C" {
+
+sdpa_status sdpa_forward(const sdpa_shape* shape, const void* q, const void* k, const void* v,
+                         const float* mask_or_null, double scale, int is_causal, int enable_gqa, void* o,
+                         float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(shape, nullptr, is_causal, q, k, v, mask_or_null, scale, enable_gqa, o, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+sdpa_status sdpa_forward_opts(const sdpa_shape* shape, const sdpa_options* options, const void* q, const void* k,
+                              const void* v, const float* mask_or_null, double scale, int enable_gqa, void* o,
+                              float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!options) return SDPA_ERR_INVALID_ARG;
+  return forward_impl(shape, options, 0, q, k, v, mask_or_null, scale, enable_gqa, o, lse, workspace,
+                      workspace_bytes, stream);
+}
+
 size_t sdpa_forward_workspace_bytes(const sdpa_shape* shape) {
   Checked c;
   if (check_shape(shape, 1, false, &c) != SDPA_OK) return 0;
-  if (!routes_to_decode(c, false, 0)) return 0;
+  if (!routes_to_decode(c)) return 0;
   int nsplit, kps;
   split_layout(c, auto_splits(c), &nsplit, &kps);
   return decode_ws(c, nsplit);
@@ -291,44 +421,24 @@ size_t sdpa_forward_workspace_bytes(const sdpa_shape* shape) {
 sdpa_status sdpa_decode(const sdpa_shape* shape, const void* q, const void* k, const void* v,
                         const float* mask_or_null, double scale, int enable_gqa, int num_splits, void* o,
                         float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  Checked c;
-  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
-  if (s != SDPA_OK) return s;
-  float alpha;
-  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
-  if (num_splits < 0) return SDPA_ERR_INVALID_ARG;
-  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      (mask_or_null && !aligned16(mask_or_null)))
-    return SDPA_ERR_INVALID_ARG;
-  if (!c.bf16 || !decode_supported(c.E, c.Ev)) return SDPA_ERR_UNSUPPORTED;
-  return run_decode(c, q, k, v, mask_or_null, alpha, num_splits, o, lse, workspace, workspace_bytes,
-                    static_cast<cudaStream_t>(stream));
+  return decode_impl(shape, nullptr, q, k, v, mask_or_null, scale, enable_gqa, num_splits, o, lse, workspace,
+                     workspace_bytes, false, stream);
+}
+
+sdpa_status sdpa_decode_opts(const sdpa_shape* shape, const sdpa_options* options, const void* q, const void* k,
+                             const void* v, const float* mask_or_null, double scale, int enable_gqa,
+                             int num_splits, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (!options) return SDPA_ERR_INVALID_ARG;
+  return decode_impl(shape, options, q, k, v, mask_or_null, scale, enable_gqa, num_splits, o, lse, workspace,
+                     workspace_bytes, false, stream);
 }
 
 sdpa_status sdpa_decode_noalloc(const sdpa_shape* shape, const void* q, const void* k, const void* v,
                                 const float* mask_or_null, double scale, int enable_gqa, int num_splits, void* o,
                                 float* lse, void* stream) {
-  Checked c;
-  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
-  if (s != SDPA_OK) return s;
-  float alpha;
-  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
-  if (num_splits < 0) return SDPA_ERR_INVALID_ARG;
-  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      (mask_or_null && !aligned16(mask_or_null)))
-    return SDPA_ERR_INVALID_ARG;
-  if (!c.bf16 || !decode_supported(c.E, c.Ev)) return SDPA_ERR_UNSUPPORTED;
-  const int want = num_splits > 0 ? num_splits : auto_splits(c);
-  int nsplit, kps;
-  split_layout(c, want, &nsplit, &kps);
-  if (decode_ws(c, nsplit) > SDPA_DECODE_STATIC_SCRATCH_BYTES) return SDPA_ERR_UNSUPPORTED;
-  void* scratch = nullptr;
-  size_t cap = 0;
-  if (decode_static_scratch(&scratch, &cap) != cudaSuccess) return SDPA_ERR_CUDA;
-  return run_decode(c, q, k, v, mask_or_null, alpha, want, o, lse, scratch, cap,
-                    static_cast<cudaStream_t>(stream));
+  return decode_impl(shape, nullptr, q, k, v, mask_or_null, scale, enable_gqa, num_splits, o, lse, nullptr, 0,
+                     true, stream);
 }
 
 size_t sdpa_decode_workspace_bytes(const sdpa_shape* shape, int num_splits) {
@@ -351,55 +461,17 @@ sdpa_status sdpa_backward(const sdpa_shape* shape, const void* q, const void* k,
                           const void* dO, const float* lse, const float* mask_or_null, double scale,
                           int is_causal, int enable_gqa, void* dq, void* dk, void* dv, void* workspace,
                           size_t workspace_bytes, void* stream) {
-  Checked c;
-  sdpa_status s = check_shape(shape, enable_gqa, mask_or_null != nullptr, &c);
-  if (s != SDPA_OK) return s;
-  float alpha;
-  if ((s = check_scale(scale, c.E, &alpha)) != SDPA_OK) return s;
-  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
-  for (const void* ptr : ptrs)
-    if (!ptr || !aligned16(ptr)) return SDPA_ERR_INVALID_ARG;
-  if (mask_or_null && !aligned16(mask_or_null)) return SDPA_ERR_INVALID_ARG;
-  const size_t need = bwd_ws(c);
-  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SDPA_ERR_INVALID_ARG;
-  BwdParams p;
-  p.q = q;
-  p.k = k;
-  p.v = v;
-  p.o = o;
-  p.dO = dO;
-  p.lse = lse;
-  p.mask = mask_or_null;
-  p.D = static_cast<float*>(workspace);
-  p.dq_acc = bwd_uses_tc(c) ? reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_stats_bytes(c))
-                            : nullptr;
-  p.dq = dq;
-  p.dk = dk;
-  p.dv = dv;
-  p.B = c.B;
-  p.Hq = c.Hq;
-  p.Hkv = c.Hkv;
-  p.L = c.L;
-  p.S = c.S;
-  p.E = c.E;
-  p.Ev = c.Ev;
-  p.G = c.G;
-  p.mask_sb = c.mask_sb;
-  p.mask_sh = c.mask_sh;
-  p.scale = alpha;
-  p.scale_log2 = alpha * kLog2e;
-  p.causal = is_causal ? 1 : 0;
-  p.status = status_ptr();
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (p.dq_acc) {
-    if (c.B * c.Hkv > 65535 * 64 || (c.S + 127) / 128 > 65535) return SDPA_ERR_UNSUPPORTED;
-    return from_cuda(launch_bwd_tc(p, st));
-  }
-  cudaError_t e = launch_bwd_preprocess(p, c.bf16 ? 1 : 0, st);
-  if (e != cudaSuccess) return SDPA_ERR_CUDA;
-  if ((c.L + 15) / 16 > 65535 || (c.S + 15) / 16 > 65535 || static_cast<long long>(c.B) * c.Hq > 65535)
-    return SDPA_ERR_UNSUPPORTED;
-  return from_cuda(launch_bwd_simt(p, c.bf16 ? 1 : 0, st));
+  return backward_impl(shape, nullptr, is_causal, q, k, v, o, dO, lse, mask_or_null, scale, enable_gqa, dq, dk, dv,
+                       workspace, workspace_bytes, stream);
+}
+
+sdpa_status sdpa_backward_opts(const sdpa_shape* shape, const sdpa_options* options, const void* q, const void* k,
+                               const void* v, const void* o, const void* dO, const float* lse,
+                               const float* mask_or_null, double scale, int enable_gqa, void* dq, void* dk,
+                               void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!options) return SDPA_ERR_INVALID_ARG;
+  return backward_impl(shape, options, 0, q, k, v, o, dO, lse, mask_or_null, scale, enable_gqa, dq, dk, dv,
+                       workspace, workspace_bytes, stream);
 }
 
 size_t sdpa_backward_workspace_bytes(const sdpa_shape* shape) {

@@ -54,10 +54,13 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
 #pragma unroll
     for (int c = 0; c < kMaxC; ++c) acc[rr][c] = 0.f;
   }
-  int kend = S;
-  if (p.causal) kend = min(S, i0 + kRows);          // key j is visible to row i only if j <= i
+  // keys any row of this block can see: lo(first row) .. hi(last row before Lb)
+  const BandRows br = band_rows(p.band, b, L, S);
+  const int ilast = min(i0 + kRows, br.Lb) - 1;
+  const int kbeg = ilast >= i0 ? br.lo(i0) / kKT * kKT : 0;
+  const int kend = ilast >= i0 ? br.hi(ilast) + 1 : 0;
 
-  for (int j0 = 0; j0 < kend; j0 += kKT) {
+  for (int j0 = kbeg; j0 < kend; j0 += kKT) {
     __syncthreads();
     for (int x = tid; x < kKT * E; x += blockDim.x) {
       const int jj = x / E, e = x - jj * E, j = j0 + jj;
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
         float s = 0.f;
         for (int e = 0; e < E; ++e) s = fmaf(sQ[r * E + e], sK[jj * KS + e], s);
         s *= p.scale;
-        if (j >= S || (p.causal && j > i)) s = neg_inf();
+        if (j >= S || !br.visible(i, j)) s = neg_inf();
         else if (mask && i < L) s += mask[static_cast<size_t>(i) * S + j];
         x[t] = s;
       }
@@ -175,9 +178,11 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
 #pragma unroll
     for (int c = 0; c < kMaxC; ++c) acc[rr][c] = 0.f;
   }
-  int kend = S;
-  if (p.causal) kend = min(S, i0 + kRows);
-  for (int j0 = 0; j0 < kend; j0 += kKT) {
+  const BandRows br = band_rows(p.band, b, L, S);
+  const int ilast = min(i0 + kRows, br.Lb) - 1;
+  const int kbeg = ilast >= i0 ? br.lo(i0) / kKT * kKT : 0;
+  const int kend = ilast >= i0 ? br.hi(ilast) + 1 : 0;
+  for (int j0 = kbeg; j0 < kend; j0 += kKT) {
     __syncthreads();
     for (int x = tid; x < kKT * E; x += blockDim.x) {
       const int jj = x / E, e = x - jj * E, j = j0 + jj;
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
       for (int t = 0; t < 2; ++t) {
         const int jj = lane + 32 * t, j = j0 + jj;
         float ds = 0.f;
-        if (j < S && !(p.causal && j > i) && lse[rr] != neg_inf()) {
+        if (j < S && br.visible(i, j) && lse[rr] != neg_inf()) {
           float s = 0.f, dp = 0.f;
           for (int e = 0; e < E; ++e) s = fmaf(sQ[r * E + e], sK[jj * KS + e], s);
           for (int e = 0; e < Ev; ++e) dp = fmaf(sDO[r * Ev + e], sV[jj * VS + e], dp);
@@ -269,13 +274,18 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
 #pragma unroll
     for (int c = 0; c < kMaxC; ++c) dk[rr][c] = dv[rr][c] = 0.f;
 
-  const int ibeg = p.causal ? (j0 / kQT) * kQT : 0;   // rows i < j0 see none of these keys
+  // rows that see a key of this block: from the first row reaching j0 to the
+  // last row whose range starts by the block's last key (before Sb)
+  const BandRows br = band_rows(p.band, b, L, S);
+  const int jlast = min(j0 + kKeys, br.Sb) - 1;
+  const int ibeg = jlast >= j0 ? br.first_row_reaching(j0) / kQT * kQT : L;
+  const int iend = jlast >= j0 ? br.last_row_starting_by(jlast) + 1 : 0;
   for (int g = 0; g < p.G; ++g) {
     const int h = hk * p.G + g, bh = b * p.Hq + h;
     const T* q = static_cast<const T*>(p.q) + static_cast<size_t>(bh) * L * E;
     const T* dO = static_cast<const T*>(p.dO) + static_cast<size_t>(bh) * L * Ev;
     const float* mask = p.mask ? p.mask + b * p.mask_sb + h * p.mask_sh : nullptr;
-    for (int it0 = ibeg; it0 < L; it0 += kQT) {
+    for (int it0 = ibeg; it0 < iend; it0 += kQT) {
       __syncthreads();
       for (int x = tid; x < kQT * E; x += blockDim.x) {
         const int r = x / E, e = x - r * E, i = it0 + r;
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
         for (int t = 0; t < 2; ++t) {
           const int r = lane + 32 * t, i = it0 + r;
           float pij = 0.f, ds = 0.f;
-          if (j < S && i < L && !(p.causal && j > i) && sL[r] != neg_inf()) {
+          if (j < S && i < L && br.visible(i, j) && sL[r] != neg_inf()) {
             float s = 0.f, dp = 0.f;
             for (int e = 0; e < E; ++e) s = fmaf(sQ[r * QS + e], sK[kk * E + e], s);
             for (int e = 0; e < Ev; ++e) dp = fmaf(sDO[r * OS + e], sV[kk * Ev + e], dp);

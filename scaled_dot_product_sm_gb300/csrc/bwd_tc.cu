@@ -200,15 +200,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Causal: grid (KV groups, key tiles), so the heaviest key tiles of every group
-  // start first.  Otherwise every CTA has the same work and the grid is (key
-  // tiles, KV groups): the key-tile CTAs of one group run side by side and share
-  // its Q/dO tiles and dQ accumulator rows in L2.
-  const int bkv = p.causal ? blockIdx.x : blockIdx.y, b = bkv / p.Hkv, hkv = bkv - b * p.Hkv;
-  const int k0 = (p.causal ? blockIdx.y : blockIdx.x) * BKV;
-  const int nqt = (p.L + BQ - 1) / BQ;
-  const int qt_begin = p.causal ? min(k0 / BQ, nqt) : 0;
-  const int per_head = nqt - qt_begin;
+  // Right-bounded (causal-like) bands: grid (KV groups, key tiles), so the
+  // heaviest key tiles of every group start first.  Otherwise every CTA has
+  // about the same work and the grid is (key tiles, KV groups): the key-tile
+  // CTAs of one group run side by side and share its Q/dO tiles and dQ
+  // accumulator rows in L2.
+  const bool right_bounded = p.band.right >= 0;
+  const int bkv = right_bounded ? blockIdx.x : blockIdx.y, b = bkv / p.Hkv, hkv = bkv - b * p.Hkv;
+  const int k0 = (right_bounded ? blockIdx.y : blockIdx.x) * BKV;
+  // query tiles that see a key of this tile: rows first_row_reaching(k0) ..
+  // last_row_starting_by(last key before Sb) (padding and band)
+  const BandRows br = band_rows(p.band, b, p.L, p.S);
+  const int klast = min(k0 + BKV, br.Sb) - 1;
+  const int i_first = klast >= k0 ? br.first_row_reaching(k0) : 1;
+  const int i_last = klast >= k0 ? br.last_row_starting_by(klast) : 0;
+  const int qt_lo = i_first / BQ, qt_hi = i_last >= i_first ? i_last / BQ : qt_lo - 1;
+  const int per_head = qt_hi - qt_lo + 1;
   const int n = p.G * per_head;                          // iterations
   // Iteration i -> (query tile, head): tiles from the last down to the diagonal,
   // the group's heads innermost.  Every CTA of a KV group starts at the same
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
-  const TileIter tile0{nqt - 1, 0, p.G};
+  const TileIter tile0{qt_hi, 0, p.G};
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -396,11 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // t = s alpha log2e + mask log2e - lse log2e
 #pragma unroll
       for (int j = 0; j < kHalf; j += 2) fma2(x[j], x[j + 1], x[j], x[j + 1], sc, sc, nl[j], nl[j + 1]);
-      // keys past S, and (causal) keys after the query: both tests are warp-uniform to skip
-      if (k0 + BKV > p.S || (p.causal && k0 + BKV - 1 > qc)) {
+      // padding and band: the per-element test only where this warp's 32 queries do
+      // not all see every key of the tile (a warp-uniform test)
+      if (!(qc + kHalf - 1 < br.Lb && br.lo(qc + kHalf - 1) <= k0 && br.hi(qc) >= k0 + BKV - 1)) {
+        // query qc + j sees this lane's key exactly for j in [jlo, jhi]:
+        // hi(qc + j) >= key, lo(qc + j) <= key and qc + j < Lb, solved for j
+        int jlo = 0, jhi = key < br.Sb ? br.Lb - 1 - qc : -1;
+        if (br.right >= 0) jlo = key - qc - br.off - br.right;
+        if (br.left > 0) jhi = min(jhi, key - qc - br.off + br.left - 1);
 #pragma unroll
         for (int j = 0; j < kHalf; ++j)
-          if (key >= p.S || (p.causal && key > qc + j)) x[j] = kNegInf;
+          if (j < jlo || j > jhi) x[j] = kNegInf;
       }
 #pragma unroll
       for (int j = 0; j < kHalf; ++j) x[j] = ex2(x[j]);     // P^T
@@ -561,7 +574,7 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) != cudaSuccess)
     return e;
   const unsigned groups = static_cast<unsigned>(p.B * p.Hkv), ktiles = static_cast<unsigned>((p.S + BKV - 1) / BKV);
-  const dim3 grid = p.causal ? dim3(groups, ktiles) : dim3(ktiles, groups);
+  const dim3 grid = p.band.right >= 0 ? dim3(groups, ktiles) : dim3(ktiles, groups);
   kern<<<grid, kThreads, C::kSmemBytes, st>>>(tmK, tmV, tmQ, tmdO, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;

@@ -15,6 +15,48 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kStatusTimeout = 4u;
 __host__ __device__ constexpr unsigned status_code(unsigned where) { return kStatusTimeout | (where << 8); }
 
+// Padding and diagonal band of a call ("Attention" (cuDNN): Configurable
+// Options, Padding mask and Diagonal masking options).  For batch b the actual
+// lengths are Lb = seq_len_q[b] and Sb = seq_len_kv[b] (clamped to [0, L] and
+// [0, S]; L and S without length arrays).  Row i < Lb sees the keys lo(i)..hi(i):
+//   diagonal d(i) = i (top-left) or i + Sb - Lb (bottom-right),
+//   hi(i) = min(Sb - 1, d(i) + right) with a right bound (0 = causal), else Sb - 1,
+//   lo(i) = max(0, d(i) - left + 1) with a left bound, else 0;
+// rows i >= Lb see nothing.  The host clamps both bounds to L + S, so the
+// arithmetic below stays within int.
+struct Band {
+  const int* seqlen_q;   // device [B] or nullptr
+  const int* seqlen_kv;  // device [B] or nullptr
+  int bottom_right;      // 1: the diagonal is aligned at the bottom-right
+  int right;             // < 0: no right bound
+  int left;              // <= 0: no left bound
+  __host__ __device__ bool restricts() const { return seqlen_q || seqlen_kv || right >= 0 || left > 0; }
+};
+
+// A Band resolved for one batch.  lo and hi are non-decreasing in i.
+struct BandRows {
+  int Lb, Sb, off, right, left;
+  __device__ __forceinline__ int hi(int i) const { return right >= 0 ? min(Sb - 1, i + off + right) : Sb - 1; }
+  __device__ __forceinline__ int lo(int i) const { return left > 0 ? max(0, i + off - left + 1) : 0; }
+  __device__ __forceinline__ bool visible(int i, int j) const { return i < Lb && j >= lo(i) && j <= hi(i); }
+  // first row whose range reaches key j (hi(i) >= j), for j < Sb
+  __device__ __forceinline__ int first_row_reaching(int j) const { return right >= 0 ? max(0, j - off - right) : 0; }
+  // last row whose range starts at or before key j (lo(i) <= j), capped at Lb - 1
+  __device__ __forceinline__ int last_row_starting_by(int j) const {
+    return left > 0 ? min(Lb - 1, j - off + left - 1) : Lb - 1;
+  }
+};
+
+__device__ __forceinline__ BandRows band_rows(const Band& bd, int b, int L, int S) {
+  BandRows r;
+  r.Lb = bd.seqlen_q ? min(max(__ldg(bd.seqlen_q + b), 0), L) : L;
+  r.Sb = bd.seqlen_kv ? min(max(__ldg(bd.seqlen_kv + b), 0), S) : S;
+  r.off = bd.bottom_right ? r.Sb - r.Lb : 0;
+  r.right = bd.right;
+  r.left = bd.left;
+  return r;
+}
+
 // Forward problem (prefill and decode).  Strides are in elements.
 struct FwdParams {
   const void* q;
@@ -28,7 +70,7 @@ struct FwdParams {
   long long mask_sh;     // element stride of the mask's head index (0 when broadcast)
   float scale;           // alpha
   float scale_log2;      // alpha * log2(e)
-  int causal;
+  Band band;             // padding and diagonal band (top-left causal = right bound 0)
   unsigned* status;
 };
 
@@ -48,7 +90,7 @@ struct BwdParams {
   int B, Hq, Hkv, L, S, E, Ev, G;
   long long mask_sb, mask_sh;
   float scale, scale_log2;
-  int causal;
+  Band band;
   unsigned* status;
 };
 

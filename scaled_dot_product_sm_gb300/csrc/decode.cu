@@ -72,10 +72,23 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
   const int nrg = (p.G * p.L + kRowsPerCta - 1) / kRowsPerCta;
   const int bk = blockIdx.y / nrg, rg = blockIdx.y - bk * nrg;   // bk = b * Hkv + hkv
   const int b = bk / p.Hkv, hk = bk - b * p.Hkv;
+  const int rows = p.G * p.L;
+  // This split's keys, cut to those the CTA's rows can see (padding and band):
+  // lo of the smallest query index .. hi of the largest one below Lb.
+  const BandRows br = band_rows(p.band, b, p.L, p.S);
+  int imin = p.L, imax = -1;
+  for (int r = rg * kRowsPerCta; r < min(rows, (rg + 1) * kRowsPerCta); ++r) {
+    const int i = r % p.L;
+    imin = min(imin, i);
+    imax = max(imax, i);
+  }
+  imax = min(imax, br.Lb - 1);
   const int k_begin = split * dp.keys_per_split;
   const int k_end = min(p.S, k_begin + dp.keys_per_split);
-  const int nst = k_end > k_begin ? (k_end - k_begin + kStageKeys - 1) / kStageKeys : 0;
-  const int rows = p.G * p.L;
+  const int k_lo = imax >= imin ? max(k_begin, br.lo(imin)) : k_end;
+  const int k_hi = imax >= imin ? min(k_end, br.hi(imax) + 1) : k_begin;
+  const int k_first = k_begin + (k_lo - k_begin) / kStageKeys * kStageKeys;   // first stage's key
+  const int nst = k_hi > k_lo ? (k_hi - k_first + kStageKeys - 1) / kStageKeys : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -97,7 +110,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         mbar_wait(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, status_code(0x21));
         uint8_t* st = smem + s * SM::kStageBytes;
         mbar_arrive_expect_tx(&full[s], SM::kStageBytes);
-        const int key0 = k_begin + it * kStageKeys;
+        const int key0 = k_first + it * kStageKeys;
 #pragma unroll
         for (int c = 0; c < ECH; ++c) tma_load_3d(st + c * kStageKeys * 128, &tmK, &full[s], c * 64, key0, bk);
 #pragma unroll
@@ -124,16 +137,16 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         qb[ks][1] = ok ? __ldg(qrow + ks * 8 + 4 + tq) : 0u;
       }
     }
-    // mask pointers of the two rows (columns) this lane owns: cols 2*tq, 2*tq+1
+    // query index and mask row of the two rows (columns) this lane owns: cols 2*tq, 2*tq+1
     const float* mrow[2] = {nullptr, nullptr};
-    if (p.mask) {
+    int irow[2] = {p.L, p.L};   // rows past the group: index L, never visible
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int r = rg * kRowsPerCta + 2 * tq + t;
-        if (r < rows) {
-          const int g = r / p.L, i = r - g * p.L;
-          mrow[t] = p.mask + b * p.mask_sb + (hk * p.G + g) * p.mask_sh + static_cast<size_t>(i) * p.S;
-        }
+    for (int t = 0; t < 2; ++t) {
+      const int r = rg * kRowsPerCta + 2 * tq + t;
+      if (r < rows) {
+        const int g = r / p.L, i = r - g * p.L;
+        irow[t] = i;
+        if (p.mask) mrow[t] = p.mask + b * p.mask_sb + (hk * p.G + g) * p.mask_sh + static_cast<size_t>(i) * p.S;
       }
     }
     float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
@@ -162,13 +175,13 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         }
       }
       // ---- scale, mask, online softmax per row (column of S^T)
-      const int key0 = k_begin + it * kStageKeys + kw + n;   // keys of c0/c1; +8 for c2/c3
+      const int key0 = k_first + it * kStageKeys + kw + n;   // keys of c0/c1; +8 for c2/c3
       float x[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int key = key0 + ((t >> 1) << 3);
         float v = c[t] * p.scale_log2;
-        if (key >= k_end) v = kNegInf;
+        if (key >= k_hi || !br.visible(irow[t & 1], key)) v = kNegInf;
         else if (mrow[t & 1]) v += mrow[t & 1][key] * kLog2e;
         x[t] = v;
       }

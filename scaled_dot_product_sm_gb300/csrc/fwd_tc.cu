@@ -106,30 +106,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k = r * G + ((r & 1) ? G - 1 - c : c);
     return k < total ? k : -1;
   };
+  // Key tiles of a unit: tile t (rows rt..rt+127) needs key tiles [a_t, b_t),
+  // from lo(rt) to hi(last row before Lb) (padding and band; empty when no row
+  // sees a key); the unit loads their union [j0, j1), which is contiguous.
   struct Unit {
-    int bh, b, h, bkv, r0, n_t[2], n;
+    int bh, b, h, bkv, r0, a[2], e[2], j0, j1;
   };
+  const bool right_bounded = p.band.right >= 0;
   auto unit_at = [&](int k) {
     Unit u;
-    // causal: row pairs outer (the last, heaviest pairs of every head first);
-    // otherwise heads outer, so the pairs of one head run side by side and share its K/V in L2
-    const int pair = p.causal ? k / BHq : k % units;
-    u.bh = p.causal ? k - pair * BHq : k / units;
+    // right-bounded (causal-like): row pairs outer (the last, heaviest pairs of every
+    // head first); otherwise heads outer, so the pairs of one head run side by side
+    // and share its K/V in L2
+    const int pair = right_bounded ? k / BHq : k % units;
+    u.bh = right_bounded ? k - pair * BHq : k / units;
     u.b = u.bh / p.Hq;
     u.h = u.bh - u.b * p.Hq;
     u.bkv = u.b * p.Hkv + u.h / p.G;
     u.r0 = (units - 1 - pair) * 2 * BM;
+    const BandRows br = band_rows(p.band, u.b, p.L, p.S);
+    u.j0 = 0x7fffffff;
+    u.j1 = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const int rt = u.r0 + t * BM;
-      if (rt >= p.L) {
-        u.n_t[t] = 0;
-      } else {
-        const int kmax = p.causal ? min(p.S, rt + BM) : p.S;
-        u.n_t[t] = (kmax + BN - 1) / BN;
+      const int rt = u.r0 + t * BM, last = min(rt + BM, br.Lb) - 1;
+      const int lo = br.lo(rt), hi = last >= rt ? br.hi(last) : -1;
+      u.a[t] = hi >= lo ? lo / BN : 0;
+      u.e[t] = hi >= lo ? hi / BN + 1 : 0;
+      if (u.e[t] > u.a[t]) {
+        u.j0 = min(u.j0, u.a[t]);
+        u.j1 = max(u.j1, u.e[t]);
       }
     }
-    u.n = max(u.n_t[0], u.n_t[1]);   // n_t[0] <= n_t[1] unless tile 1 is past L
+    if (u.j1 == 0) u.j0 = 0;
     return u;
   };
 
@@ -170,15 +179,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit u = unit_at(k);
         // the previous unit's S MMAs have read its Q tiles
         mbar_wait(q_free, (r & 1) ^ 1, abort_flag, p.status, status_code(0x10));
-        const int nq = (u.n_t[0] > 0) + (u.n_t[1] > 0);
-        mbar_arrive_expect_tx(bar_q, nq * C::kQBytes);
+        const int nq = (u.e[0] > u.a[0]) + (u.e[1] > u.a[1]);
+        mbar_arrive_expect_tx(bar_q, nq * C::kQBytes);   // no tiles: a plain arrival
         for (int t = 0; t < 2; ++t) {
-          if (u.n_t[t] == 0) continue;
+          if (u.e[t] == u.a[t]) continue;
           for (int c = 0; c < ECH; ++c)
             tma_load_3d(smem + C::kOffQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar_q, c * 64, u.r0 + t * BM,
                         u.bh);
         }
-        // ring order = consumption order: K_0, then per j: V_j, K_{j+1} (if any)
+        // ring order = consumption order: K_j0, then per j: V_j, K_{j+1} (if any)
         auto load = [&](bool is_k, int j) {
           const int s = it % NS;
           mbar_wait(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.status, status_code(0x11));
@@ -189,10 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(dst + c * kChunkBytes, is_k ? &tmK : &tmV, &full[s], c * 64, j * BN, u.bkv);
           ++it;
         };
-        load(true, 0);
-        for (int j = 0; j < u.n; ++j) {
+        if (u.j1 > u.j0) load(true, u.j0);
+        for (int j = u.j0; j < u.j1; ++j) {
           load(false, j);
-          if (j + 1 < u.n) load(true, j + 1);
+          if (j + 1 < u.j1) load(true, j + 1);
         }
       }
     } else if (warp == 9 && lane == 0) {
@@ -225,32 +234,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k < 0) break;
         const Unit u = unit_at(k);
         mbar_wait(bar_q, r & 1, abort_flag, p.status, status_code(0x12));
+        if (u.j1 == u.j0) {
+          umma_commit(q_free);   // nothing to compute; covers the earlier units' MMAs
+          continue;
+        }
         {
           const int s = it % NS;
           mbar_wait(&full[s], (it / NS) & 1, abort_flag, p.status, status_code(0x13));
           tc_fence_after();
           for (int t = 0; t < 2; ++t) {
-            if (u.n_t[t] == 0) continue;
+            if (u.a[t] != u.j0 || u.e[t] == u.a[t]) continue;
             issue_s(t, s);
             umma_commit(&s_full[t]);
           }
           umma_commit(&empty[s]);
-          if (u.n == 1) umma_commit(q_free);
+          if (u.j1 - u.j0 == 1) umma_commit(q_free);
           ++it;
         }
-        for (int j = 0; j < u.n; ++j) {
+        for (int j = u.j0; j < u.j1; ++j) {
           const int sv = it % NS;
           mbar_wait(&full[sv], (it / NS) & 1, abort_flag, p.status, status_code(0x14));
           tc_fence_after();
           ++it;
           int sk = -1;
           for (int t = 0; t < 2; ++t) {
-            if (j >= u.n_t[t]) continue;
-            mbar_wait(&p_full[t], pc[t] & 1, abort_flag, p.status, status_code(0x15));
-            ++pc[t];
-            tc_fence_after();
-            issue_pv(t, sv, j > 0);
-            if (j + 1 < u.n_t[t]) {
+            const bool pv = u.a[t] <= j && j < u.e[t];
+            if (pv) {
+              mbar_wait(&p_full[t], pc[t] & 1, abort_flag, p.status, status_code(0x15));
+              ++pc[t];
+              tc_fence_after();
+              issue_pv(t, sv, j > u.a[t]);
+            }
+            if (u.a[t] <= j + 1 && j + 1 < u.e[t]) {
               if (sk < 0) {
                 sk = it % NS;
                 mbar_wait(&full[sk], (it / NS) & 1, abort_flag, p.status, status_code(0x16));
@@ -259,13 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               issue_s(t, sk);   // overwrites P_t(j) after PV_t(j) in issue order
               umma_commit(&s_full[t]);
-            } else {
+            } else if (pv) {
               umma_commit(&o_final[t]);
             }
           }
+          if (j + 1 < u.j1 && sk < 0) {   // K_{j+1} is in the ring for the other tile only: release it
+            sk = it % NS;
+            mbar_wait(&full[sk], (it / NS) & 1, abort_flag, p.status, status_code(0x16));
+            ++it;
+          }
           umma_commit(&empty[sv]);
           if (sk >= 0) umma_commit(&empty[sk]);
-          if (j + 2 == u.n) umma_commit(q_free);   // the unit's last S MMAs were just issued
+          if (j + 2 == u.j1) umma_commit(q_free);   // the unit's last S MMAs were just issued
         }
       }
     }
@@ -284,17 +304,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k = unit_index(ur);
       if (k < 0) break;
       const Unit u = unit_at(k);
-      const int nt = u.n_t[t];
-      if (nt == 0) continue;
       const int row_first = u.r0 + t * BM;   // first row of this tile
       const int row = row_first + r;
+      if (row_first >= p.L) continue;
+      const int ja = t ? u.a[1] : u.a[0], je = t ? u.e[1] : u.e[0];
+      if (je == ja) {   // no row of this tile sees a key: o = 0, lse = -inf
+        if (row < p.L) {
+          __nv_bfloat16* orow =
+              static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(u.bh) * p.L + row) * C::Ev;
+#pragma unroll
+          for (int c = 0; c < C::Ev / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[static_cast<size_t>(u.bh) * p.L + row] = kNegInf;
+        }
+        continue;
+      }
+      const BandRows br = band_rows(p.band, u.b, p.L, p.S);
+      // the tile's rows all see every key of a key tile inside [lo(last row), hi(first row)]
+      const int row_last = row_first + BM - 1;
+      const bool rows_full = row_last < br.Lb;
+      const int full_lo = rows_full ? br.lo(row_last) : 0x7fffffff, full_hi = br.hi(row_first);
       // 256-bit mask loads need 32-byte aligned rows: base aligned and S a multiple of 8
       const bool mask_v8 = (reinterpret_cast<uintptr_t>(p.mask) & 31) == 0 && (p.S & 7) == 0;
       const float* mrow = (p.mask && row < p.L)
                               ? p.mask + u.b * p.mask_sb + u.h * p.mask_sh + static_cast<size_t>(row) * p.S
                               : nullptr;
       float m_run = kNegInf, l_run = 0.f;
-      for (int j = 0; j < nt; ++j) {
+      for (int j = ja; j < je; ++j) {
         const int kb = j * BN;
         float x[BN];
         if (MASKED) {   // the TMEM loads below are executed by the whole warp in either branch
@@ -357,15 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BN; i += 2)
             mul2(x[i], x[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sc, sc);
         }
-        if (kb + BN > p.S) {
+        if (!(kb >= full_lo && kb + BN - 1 <= full_hi)) {   // warp-uniform: the tile crosses a boundary
+          // this row sees key kb + i exactly for i in [ilo, ihi]
+          const int ilo = br.lo(row) - kb, ihi = row < br.Lb ? br.hi(row) - kb : -1;
 #pragma unroll
           for (int i = 0; i < BN; ++i)
-            if (kb + i >= p.S) x[i] = kNegInf;
-        }
-        if (p.causal && kb + BN - 1 > row_first) {
-#pragma unroll
-          for (int i = 0; i < BN; ++i)
-            if (kb + i > row) x[i] = kNegInf;
+            if (i < ilo || i > ihi) x[i] = kNegInf;
         }
         // row max: eight independent chains of three-input maxima
         float mx8[8];
@@ -397,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l_run = l_run * corr + rs;
-        if (j > 0) {
-          // O_t holds PV_t(0..j-1) (complete: the commit after S_t(j) covered it)
+        if (j > ja) {
+          // O_t holds PV_t(ja..j-1) (complete: the commit after S_t(j) covered it)
           if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
             for (int c = 0; c < C::Ev / 32; ++c) {

@@ -142,3 +142,43 @@ def test_binding_requires_cuda_tensors():
     q = torch.zeros(1, 1, 4, 8)
     with pytest.raises(ValueError):
         sdpa.sdpa_forward(q, q, q)
+
+
+def _fwd_opts(lib, shp, opts):
+    return lib.sdpa_forward_opts(ctypes.byref(shp), opts, P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 0,
+                                 P(FAKE), P(FAKE), None, 0, None)
+
+
+def test_opts_entry_points_reject_bad_options(lib):
+    shp = _shape()
+    # options are required by the *_opts calls
+    assert _fwd_opts(lib, shp, None) == INVALID
+    assert lib.sdpa_backward_opts(ctypes.byref(shp), None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                  None, float("nan"), 0, P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1 << 20,
+                                  None) == INVALID
+    dshp = _shape(L=1)
+    assert lib.sdpa_decode_opts(ctypes.byref(dshp), None, P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 0, 0,
+                                P(FAKE), P(FAKE), P(FAKE), 1 << 30, None) == INVALID
+    # an alignment other than top-left / bottom-right, and misaligned length arrays
+    bad_align = sdpa.Options(None, None, 2, -1, 0)
+    assert _fwd_opts(lib, shp, ctypes.byref(bad_align)) == INVALID
+    mis_q = sdpa.Options(FAKE + 2, None, 0, 0, 0)
+    assert _fwd_opts(lib, shp, ctypes.byref(mis_q)) == INVALID
+    mis_kv = sdpa.Options(None, FAKE + 1, 1, 0, 4)
+    assert _fwd_opts(lib, shp, ctypes.byref(mis_kv)) == INVALID
+    # shape errors still come first
+    ok = sdpa.Options(None, None, 1, 0, 16)
+    assert _fwd_opts(lib, _shape(B=0), ctypes.byref(ok)) == INVALID
+
+
+def test_binding_band_options():
+    b = sdpa.Band(alignment="bottom_right", right_bound=0, left_bound=128)
+    o = b.options()
+    assert (o.seq_len_q, o.seq_len_kv, o.diagonal_alignment, o.right_bound, o.left_bound) == (None, None, 1, 0, 128)
+    o = sdpa.Band().options()
+    assert (o.diagonal_alignment, o.right_bound, o.left_bound) == (0, -1, 0)
+    with pytest.raises(ValueError):
+        sdpa.Band(alignment="center").options()
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):   # lengths must be CUDA int32
+        sdpa.Band(seq_len_q=torch.zeros(2, dtype=torch.int32)).options()

@@ -17,7 +17,11 @@ Recipe (the same for every workload):
 
 Workload shapes follow the five benchmark configurations of this project
 (tiny fp32, MHA causal E=64, GQA causal E=128, padded + additive mask,
-GQA decode).
+GQA decode), plus two that use padding lengths and a diagonal band instead of
+a mask: the padded workload's shapes and lengths as seq_len_q = seq_len_kv
+(no mask tensor), and the GQA causal workload with a sliding window.  Their
+lengths are drawn at the padded workload's place in the draw order (after
+Q, K, V, dO) with the same distribution.
 """
 from __future__ import annotations
 
@@ -27,7 +31,7 @@ from typing import Optional
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "make_padded_bias_mask"]
+__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "make_band", "make_padded_bias_mask"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -47,6 +51,8 @@ class Workload:
     mask: str               # "none" or "padded_bias"
     phases: tuple           # ("fwd", "bwd") or ("fwd",)
     description: str = ""
+    band: str = "none"      # "none", "seqlen" (lengths U{256..S} as seq_len_q = seq_len_kv) or "window"
+    window: int = 0         # left bound of the "window" band (causal about the top-left diagonal)
 
     @property
     def torch_dtype(self):
@@ -88,6 +94,15 @@ WORKLOADS = {
         is_causal=False, enable_gqa=False, scale=None, mask="padded_bias",
         phases=("fwd", "bwd"),
         description="padded variable-length with an additive fp32 mask"),
+    "padded_seqlen_e128": Workload(
+        "padded_seqlen_e128", B=8, Hq=16, Hkv=16, L=2048, S=2048, E=128, Ev=128, dtype="bf16",
+        is_causal=False, enable_gqa=False, scale=None, mask="none", phases=("fwd", "bwd"),
+        description="padded variable-length batch given as seq_len_q / seq_len_kv (no mask tensor)",
+        band="seqlen"),
+    "gqa_swa_e128": Workload(
+        "gqa_swa_e128", B=2, Hq=32, Hkv=8, L=4096, S=4096, E=128, Ev=128, dtype="bf16",
+        is_causal=False, enable_gqa=True, scale=1.0 / math.sqrt(128), mask="none", phases=("fwd", "bwd"),
+        description="GQA causal bf16 with a sliding window of 1024 keys", band="window", window=1024),
     "gqa_decode_s32k": Workload(
         "gqa_decode_s32k", B=16, Hq=32, Hkv=8, L=1, S=32768, E=128, Ev=128, dtype="bf16",
         is_causal=False, enable_gqa=True, scale=1.0 / math.sqrt(128), mask="none",
@@ -129,6 +144,25 @@ def make_padded_bias_mask(gen: torch.Generator, B: int, L: int, S: int,
         rows = torch.randperm(L, generator=gen)[:n_rows]
         bias[b, :, rows, :] = ninf
     return bias, lengths
+
+
+def make_band(w: Workload, seed: int = 0):
+    """The workload's padding lengths and band as a dict (None when it has none).
+
+    Lengths are drawn with the generator advanced past Q, K, V and dO, exactly
+    where the padded workload draws its lengths, from the same U{256, ..., S}.
+    """
+    if w.band == "none":
+        return None
+    if w.band == "window":
+        return {"seq_len_q": None, "seq_len_kv": None, "alignment": "top_left", "right_bound": 0,
+                "left_bound": w.window}
+    gen = torch.Generator().manual_seed(seed)
+    for shape in ((w.B, w.Hq, w.L, w.E), (w.B, w.Hkv, w.S, w.E), (w.B, w.Hkv, w.S, w.Ev), (w.B, w.Hq, w.L, w.Ev)):
+        torch.randn(*shape, generator=gen)
+    lengths = [int(x) for x in torch.randint(256, w.S + 1, (w.B,), generator=gen)]
+    return {"seq_len_q": lengths, "seq_len_kv": lengths, "alignment": "top_left", "right_bound": None,
+            "left_bound": None}
 
 
 def make_inputs(w: Workload, seed: int = 0, with_grad: bool = True):
