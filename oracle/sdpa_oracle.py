@@ -35,7 +35,11 @@ Sources for each step (page title, section):
     at or before row - left_bound masked): "Attention" (cuDNN), Configurable
     Options (Padding mask, Diagonal masking options) and Scaled Dot Product
     Attention, Args (seq_len_q, seq_len_kv, diagonal_alignment,
-    diagonal_band_left_bound, diagonal_band_right_bound).
+    diagonal_band_left_bound, diagonal_band_right_bound);
+  * paged K/V caches: K_cache[b, h, s, d] = K_container[page_table_k[b, s / bs_k],
+    h, s mod bs_k, d], likewise V, with containers (num_blocks, H, bs, D) and
+    page tables (B, ceil(S / bs)): "Attention" (cuDNN), Configurable Options
+    (Paged attention, Offset calculation) and Tensors (Page Table K / V).
 
 Readings where the pages are silent (every one also listed in the design notes):
   * a fully blocked row has LSE = -inf, O = 0, dQ = 0 and contributes nothing
@@ -58,7 +62,7 @@ import numpy as np
 
 __all__ = [
     "default_scale", "ref_forward", "ref_backward", "ref_forward_rows",
-    "ref_group", "causal_bias", "band_bias", "Band",
+    "ref_group", "causal_bias", "band_bias", "Band", "gather_paged", "ref_forward_paged",
 ]
 
 NEG_INF = -np.inf
@@ -347,3 +351,37 @@ def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False, band=N
         dQ, dK, dV = ref_backward(qg, kg, vg, dOg, mg, scale, is_causal, enable_gqa=True, band=bg)
         out += [dQ[0], dK[0, 0], dV[0, 0]]
     return tuple(out)
+
+
+def gather_paged(container, page_table, block_size: int, S: int) -> np.ndarray:
+    """Dense cache [B, H, S, D] of a paged container [num_blocks, H, block_size, D].
+
+    cache[b, h, s, d] = container[page_table[b, s // block_size], h, s % block_size, d]
+    (cuDNN "Attention", Paged attention, Offset calculation).  A table entry
+    outside [0, num_blocks), or a block index past the table's width, gives
+    zeros: such positions lie past the sequence's length and are masked.
+    """
+    c = _as64(container)
+    table = np.asarray(page_table.cpu() if hasattr(page_table, "cpu") else page_table, dtype=np.int64)
+    nb, H, bs, D = c.shape
+    if bs != block_size:
+        raise ValueError("container block size differs from block_size")
+    B = table.shape[0]
+    out = np.zeros((B, H, S, D))
+    for b in range(B):
+        for s in range(S):
+            blk = s // block_size
+            if blk >= table.shape[1]:
+                continue
+            page = int(table[b, blk])
+            if 0 <= page < nb:
+                out[b, :, s, :] = c[page, :, s % block_size, :]
+    return out
+
+
+def ref_forward_paged(q, k_container, v_container, page_table_k, page_table_v, block_size_k: int,
+                      block_size_v: int, S: int, mask=None, scale=None, enable_gqa=False, band=None):
+    """Forward (O, LSE) with paged K/V: the plain forward on the gathered caches."""
+    k = gather_paged(k_container, page_table_k, block_size_k, S)
+    v = gather_paged(v_container, page_table_v, block_size_v, S)
+    return ref_forward(q, k, v, mask, scale, False, enable_gqa, band=band)
