@@ -238,6 +238,40 @@ sdpa_status sdpa_decode_opts(const sdpa_shape* shape, const sdpa_options* option
                              void* workspace, size_t workspace_bytes,
                              void* stream /* cudaStream_t */);
 
+/* Paged K/V caches of sdpa_decode_paged (cuDNN "Attention": Configurable
+ * Options, Paged attention; Tensors, Page Table K / V).  k and v are then
+ * containers of fixed-size key blocks, k [num_blocks_k, Hkv, block_size_k, E]
+ * and v [num_blocks_v, Hkv, block_size_v, Ev] (bf16, dense, 16-byte aligned),
+ * and key s of batch b is
+ *     k_cache[b, h, s, :] = k[page_table_k[b * max_blocks + s / block_size_k], h, s % block_size_k, :]
+ * (likewise v).  page_table_k / page_table_v: DEVICE int32 arrays of
+ * B * max_blocks entries, 4-byte aligned (they may be the same array).
+ * block_size_k / block_size_v: powers of two, at least 8.  max_blocks: the
+ * tables' row length, at least ceil(S / block_size) for both.  An entry that
+ * is negative or >= num_blocks reads zeros (use it for blocks past a
+ * sequence's length, which seq_len_kv masks anyway).  Bad fields -> INVALID_ARG. */
+typedef struct {
+  const int32_t* page_table_k;
+  const int32_t* page_table_v;
+  int32_t block_size_k;
+  int32_t block_size_v;
+  int32_t max_blocks;
+  int64_t num_blocks_k;
+  int64_t num_blocks_v;
+} sdpa_paged_kv;
+
+/* sdpa_decode_opts over paged K/V caches.  shape->S is the longest cache (the
+ * logical key length); options may be NULL and usually give seq_len_kv, each
+ * sequence's cache length.  Same workspace, results and errors as
+ * sdpa_decode. */
+sdpa_status sdpa_decode_paged(const sdpa_shape* shape, const sdpa_options* options, const sdpa_paged_kv* paged,
+                              const void* q, const void* k_container, const void* v_container,
+                              const float* mask_or_null, double scale, int enable_gqa,
+                              int num_splits,
+                              void* o, float* lse,
+                              void* workspace, size_t workspace_bytes,
+                              void* stream /* cudaStream_t */);
+
 /* Static, NUL-terminated description of a status code. */
 const char* sdpa_status_string(sdpa_status status);
 

@@ -19,7 +19,8 @@ from .build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "SdpaError", "load_library", "exported_symbols", "sdpa_forward", "sdpa_backward", "sdpa_decode",
     "forward_workspace_bytes", "backward_workspace_bytes", "decode_workspace_bytes",
-    "decode_num_splits", "last_device_status", "Shape", "Options", "Band", "build", "LIB_PATH",
+    "decode_num_splits", "last_device_status", "Shape", "Options", "Band", "PagedKV", "sdpa_decode_paged",
+    "build", "LIB_PATH",
 ]
 
 SDPA_F32, SDPA_BF16 = 0, 1
@@ -30,7 +31,7 @@ EXPORTS = (
     "sdpa_forward", "sdpa_forward_workspace_bytes", "sdpa_backward", "sdpa_backward_workspace_bytes",
     "sdpa_decode", "sdpa_decode_workspace_bytes", "sdpa_decode_num_splits", "sdpa_status_string",
     "sdpa_last_device_status", "sdpa_decode_noalloc", "sdpa_forward_opts", "sdpa_backward_opts",
-    "sdpa_decode_opts",
+    "sdpa_decode_opts", "sdpa_decode_paged",
 )
 
 
@@ -79,6 +80,13 @@ class Band:
                        0 if self.left_bound is None else int(self.left_bound))
 
 
+class PagedKV(ctypes.Structure):
+    """sdpa_paged_kv: page tables (device int32 [B * max_blocks]), block sizes, table width, container sizes."""
+    _fields_ = [("page_table_k", ctypes.c_void_p), ("page_table_v", ctypes.c_void_p),
+                ("block_size_k", ctypes.c_int32), ("block_size_v", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("num_blocks_k", ctypes.c_int64), ("num_blocks_v", ctypes.c_int64)]
+
+
 _lib = None
 _P = ctypes.c_void_p
 
@@ -115,6 +123,9 @@ def load_library(path: Optional[str] = None):
     lib.sdpa_decode_opts.argtypes = [SP, OP, _P, _P, _P, _P, ctypes.c_double, ctypes.c_int, ctypes.c_int, _P, _P,
                                      _P, ctypes.c_size_t, _P]
     lib.sdpa_decode_opts.restype = ctypes.c_int
+    lib.sdpa_decode_paged.argtypes = [SP, OP, ctypes.POINTER(PagedKV), _P, _P, _P, _P, ctypes.c_double, ctypes.c_int,
+                                      ctypes.c_int, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.sdpa_decode_paged.restype = ctypes.c_int
     for fn in ("sdpa_forward_workspace_bytes", "sdpa_backward_workspace_bytes"):
         getattr(lib, fn).argtypes = [SP]
         getattr(lib, fn).restype = ctypes.c_size_t
@@ -304,6 +315,43 @@ def sdpa_decode(q, k, v, mask=None, scale=None, enable_gqa=False, num_splits=0,
                          int(bool(enable_gqa)), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace), wsb,
                          _stream(stream))
     _raise(st, "sdpa_decode")
+    return out, lse
+
+
+def sdpa_decode_paged(q, k_container, v_container, page_table_k, page_table_v, S, mask=None, scale=None,
+                      enable_gqa=False, num_splits=0, band=None, out=None, lse=None, workspace=None, stream=None):
+    """Split-KV decode over paged caches (bf16).
+
+    k_container [num_blocks_k, Hkv, bs_k, E], v_container [num_blocks_v, Hkv, bs_v, Ev];
+    page tables CUDA int32 [B, max_blocks]; S = the longest cache; band usually
+    carries seq_len_kv (each sequence's cache length).
+    """
+    import torch
+    lib = load_library()
+    _check_tensors(q, k_container, v_container, mask, page_table_k, page_table_v)
+    for t in (page_table_k, page_table_v):
+        if t.dtype != torch.int32 or t.dim() != 2 or t.shape[0] != q.shape[0]:
+            raise ValueError("page tables must be int32 [B, max_blocks]")
+    if page_table_k.shape != page_table_v.shape:
+        raise ValueError("page tables must have the same shape")
+    B, Hq, L, E = q.shape
+    Hkv, Ev = k_container.shape[1], v_container.shape[3]
+    mb, mh = (1, 1) if mask is None else (mask.shape[0], mask.shape[1])
+    shp = Shape(B, Hq, Hkv, L, int(S), E, Ev, _dtype_code(q), mb, mh)
+    paged = PagedKV(_ptr(page_table_k), _ptr(page_table_v), k_container.shape[2], v_container.shape[2],
+                    page_table_k.shape[1], k_container.shape[0], v_container.shape[0])
+    opts = (band or Band()).options()
+    if out is None:
+        out = torch.empty(B, Hq, L, Ev, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(lib.sdpa_decode_workspace_bytes(ctypes.byref(shp), int(num_splits)), q.device)
+    st = lib.sdpa_decode_paged(ctypes.byref(shp), ctypes.byref(opts), ctypes.byref(paged), _ptr(q),
+                               _ptr(k_container), _ptr(v_container), _ptr(mask), _scale(scale), int(bool(enable_gqa)),
+                               int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(st, "sdpa_decode_paged")
     return out, lse
 
 

@@ -208,7 +208,7 @@ size_t bwd_ws(const Checked& c) {
 
 sdpa_status run_decode(const Checked& c, const Band& band, const void* q, const void* k, const void* v,
                        const float* mask, float alpha, int num_splits, void* o, float* lse, void* ws,
-                       size_t ws_bytes, cudaStream_t st) {
+                       size_t ws_bytes, cudaStream_t st, const sdpa_paged_kv* paged = nullptr) {
   int nsplit, kps;
   split_layout(c, num_splits > 0 ? num_splits : auto_splits(c), &nsplit, &kps);
   if (c.B * c.Hkv * ((c.G * c.L + decode_rows_per_cta() - 1) / decode_rows_per_cta()) > 65535)
@@ -223,6 +223,13 @@ sdpa_status run_decode(const Checked& c, const Band& band, const void* q, const 
                                          round_up(rows * nsplit * c.Ev * sizeof(float), 256));
   dp.nsplit = nsplit;
   dp.keys_per_split = kps;
+  dp.page_k = paged ? paged->page_table_k : nullptr;
+  dp.page_v = paged ? paged->page_table_v : nullptr;
+  dp.page_stride = paged ? paged->max_blocks : 0;
+  dp.bs_k = paged ? paged->block_size_k : 0;
+  dp.bs_v = paged ? paged->block_size_v : 0;
+  dp.nblk_k = paged ? static_cast<int>(paged->num_blocks_k) : 0;
+  dp.nblk_v = paged ? static_cast<int>(paged->num_blocks_v) : 0;
   return from_cuda(launch_decode(dp, st));
 }
 
@@ -306,9 +313,26 @@ sdpa_status forward_impl(const sdpa_shape* shape, const sdpa_options* opts, int 
   return from_cuda(launch_fwd_simt(p, c.bf16 ? 1 : 0, st));
 }
 
+// A paged cache description: both tables present and 4-byte aligned, block sizes powers of
+// two >= 8, tables wide enough for S keys, container indices within int.
+sdpa_status check_paged(const sdpa_paged_kv* pg, const Checked& c) {
+  if (!pg || !pg->page_table_k || !pg->page_table_v) return SDPA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(pg->page_table_k) & 3) || (reinterpret_cast<uintptr_t>(pg->page_table_v) & 3))
+    return SDPA_ERR_INVALID_ARG;
+  for (int bs : {pg->block_size_k, pg->block_size_v})
+    if (bs < 8 || bs > (1 << 20) || (bs & (bs - 1))) return SDPA_ERR_INVALID_ARG;
+  const long long need_k = (static_cast<long long>(c.S) + pg->block_size_k - 1) / pg->block_size_k;
+  const long long need_v = (static_cast<long long>(c.S) + pg->block_size_v - 1) / pg->block_size_v;
+  if (pg->max_blocks < need_k || pg->max_blocks < need_v) return SDPA_ERR_INVALID_ARG;
+  for (long long nb : {pg->num_blocks_k, pg->num_blocks_v})
+    if (nb < 1 || (nb + 1) * c.Hkv > INT_MAX) return SDPA_ERR_INVALID_ARG;
+  return SDPA_OK;
+}
+
 sdpa_status decode_impl(const sdpa_shape* shape, const sdpa_options* opts, const void* q, const void* k,
                         const void* v, const float* mask, double scale, int enable_gqa, int num_splits, void* o,
-                        float* lse, void* workspace, size_t workspace_bytes, bool static_scratch, void* stream) {
+                        float* lse, void* workspace, size_t workspace_bytes, bool static_scratch, void* stream,
+                        const sdpa_paged_kv* paged = nullptr) {
   Checked c;
   sdpa_status s = check_shape(shape, enable_gqa, mask != nullptr, &c);
   if (s != SDPA_OK) return s;
@@ -318,6 +342,7 @@ sdpa_status decode_impl(const sdpa_shape* shape, const sdpa_options* opts, const
   if ((s = check_io(c, q, k, v, mask, o, lse)) != SDPA_OK) return s;
   Band band = plain_band(0);
   if (opts && (s = band_from_options(opts, c, &band)) != SDPA_OK) return s;
+  if (paged && (s = check_paged(paged, c)) != SDPA_OK) return s;
   if (!c.bf16 || !decode_supported(c.E, c.Ev)) return SDPA_ERR_UNSUPPORTED;
   const int want = num_splits > 0 ? num_splits : auto_splits(c);
   if (static_scratch) {
@@ -329,7 +354,7 @@ sdpa_status decode_impl(const sdpa_shape* shape, const sdpa_options* opts, const
     workspace_bytes = cap;
   }
   return run_decode(c, band, q, k, v, mask, alpha, want, o, lse, workspace, workspace_bytes,
-                    static_cast<cudaStream_t>(stream));
+                    static_cast<cudaStream_t>(stream), paged);
 }
 
 sdpa_status backward_impl(const sdpa_shape* shape, const sdpa_options* opts, int is_causal, const void* q,
@@ -432,6 +457,15 @@ sdpa_status sdpa_decode_opts(const sdpa_shape* shape, const sdpa_options* option
   if (!options) return SDPA_ERR_INVALID_ARG;
   return decode_impl(shape, options, q, k, v, mask_or_null, scale, enable_gqa, num_splits, o, lse, workspace,
                      workspace_bytes, false, stream);
+}
+
+sdpa_status sdpa_decode_paged(const sdpa_shape* shape, const sdpa_options* options, const sdpa_paged_kv* paged,
+                              const void* q, const void* k_container, const void* v_container,
+                              const float* mask_or_null, double scale, int enable_gqa, int num_splits, void* o,
+                              float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!paged) return SDPA_ERR_INVALID_ARG;
+  return decode_impl(shape, options, q, k_container, v_container, mask_or_null, scale, enable_gqa, num_splits, o,
+                     lse, workspace, workspace_bytes, false, stream, paged);
 }
 
 sdpa_status sdpa_decode_noalloc(const sdpa_shape* shape, const void* q, const void* k, const void* v,

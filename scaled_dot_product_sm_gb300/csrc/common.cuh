@@ -100,6 +100,13 @@ struct DecodeParams {
   float* part_lse;       // [B*Hq*L, nsplit]     fp32: partial log2-sum-exp (log2 units)
   int nsplit;
   int keys_per_split;    // multiple of the decode stage
+  // Paged caches (f.k / f.v are then containers [nblk, Hkv, bs, E|Ev]); page_k == nullptr: dense.
+  // Key s of batch b is row s % bs of block page[b * page_stride + s / bs].
+  const int* page_k;
+  const int* page_v;
+  int page_stride;       // entries per table row (>= ceil(S / bs))
+  int bs_k, bs_v;        // keys per block, powers of two >= 8
+  int nblk_k, nblk_v;    // blocks in the containers
 };
 
 __device__ __forceinline__ float to_f(float x) { return x; }

@@ -6,7 +6,9 @@
 // up to 8 rows, key split):
 //  * a producer warp streams 64-key stages of K and V into shared memory with
 //    TMA tensor copies (128-byte swizzle, so the tensor-core operand reads
-//    below are free of bank conflicts), NSTAGE stages in flight;
+//    below are free of bank conflicts), NSTAGE stages in flight; with paged
+//    caches it looks each stage's blocks up in the page table and copies from
+//    the containers (one box per min(block size, 64) keys);
 //  * four consumer warps each take 16 keys of a stage and compute the scores
 //    of all rows at once as S^T = K Q^T with warp-level bf16 MMAs (rows are the
 //    MMA's N = 8 side: the group's 4 query heads share every K/V byte read),
@@ -20,6 +22,7 @@
 // contributing nothing and an all-empty row giving o = 0, lse = -inf.
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -111,11 +114,35 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         uint8_t* st = smem + s * SM::kStageBytes;
         mbar_arrive_expect_tx(&full[s], SM::kStageBytes);
         const int key0 = k_first + it * kStageKeys;
+        if (!dp.page_k) {
 #pragma unroll
-        for (int c = 0; c < ECH; ++c) tma_load_3d(st + c * kStageKeys * 128, &tmK, &full[s], c * 64, key0, bk);
+          for (int c = 0; c < ECH; ++c) tma_load_3d(st + c * kStageKeys * 128, &tmK, &full[s], c * 64, key0, bk);
 #pragma unroll
-        for (int c = 0; c < VCH; ++c)
-          tma_load_3d(st + SM::kKBytes + c * kStageKeys * 128, &tmV, &full[s], c * 64, key0, bk);
+          for (int c = 0; c < VCH; ++c)
+            tma_load_3d(st + SM::kKBytes + c * kStageKeys * 128, &tmV, &full[s], c * 64, key0, bk);
+        } else {
+          // Paged: keys key0.. of this stage come from the container blocks the table names;
+          // a box covers min(bs, 64) keys and lands on a 1024-byte (8-row) boundary, so the
+          // 128-byte swizzle of the stage is the same as with one 64-row box.  An entry past
+          // the table or outside the container becomes block nblk: past the tensor map, so the
+          // copy fills zeros (those keys lie past the sequence's length and are masked).
+#pragma unroll 1
+          for (int kv = 0; kv < 2; ++kv) {
+            const int bs = kv ? dp.bs_v : dp.bs_k, nblk = kv ? dp.nblk_v : dp.nblk_k;
+            const int* table = (kv ? dp.page_v : dp.page_k) + static_cast<size_t>(b) * dp.page_stride;
+            const int rows_box = min(bs, kStageKeys), nch = kv ? VCH : ECH;
+            uint8_t* dst0 = st + (kv ? SM::kKBytes : 0);
+            for (int sub = 0; sub < kStageKeys / rows_box; ++sub) {
+              const int key = key0 + sub * rows_box, blk = key / bs;
+              int page = blk < dp.page_stride ? __ldg(table + blk) : nblk;
+              if (page < 0 || page >= nblk) page = nblk;
+              const int z = page * p.Hkv + hk;
+              for (int c = 0; c < nch; ++c)
+                tma_load_3d(dst0 + c * kStageKeys * 128 + sub * rows_box * 128, kv ? &tmV : &tmK, &full[s], c * 64,
+                            key & (bs - 1), z);
+            }
+          }
+        }
       }
     }
   } else {
@@ -335,10 +362,18 @@ cudaError_t run(const DecodeParams& dp, cudaStream_t st) {
   using SM = DecodeSmem<ECH, VCH, NSTAGE>;
   const FwdParams& p = dp.f;
   alignas(64) CUtensorMap tmK, tmV;
-  if (!encode_tmap_bf16_3d(&tmK, p.k, ECH * 64, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, kStageKeys))
-    return cudaErrorInvalidValue;
-  if (!encode_tmap_bf16_3d(&tmV, p.v, VCH * 64, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, kStageKeys))
-    return cudaErrorInvalidValue;
+  if (!dp.page_k) {
+    if (!encode_tmap_bf16_3d(&tmK, p.k, ECH * 64, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, kStageKeys))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_3d(&tmV, p.v, VCH * 64, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, kStageKeys))
+      return cudaErrorInvalidValue;
+  } else {   // containers [nblk, Hkv, bs, E|Ev] as (E|Ev, bs, nblk * Hkv), boxes of min(bs, 64) rows
+    if (!encode_tmap_bf16_3d(&tmK, p.k, ECH * 64, dp.bs_k, static_cast<uint64_t>(dp.nblk_k) * p.Hkv, 64,
+                             std::min(dp.bs_k, kStageKeys)) ||
+        !encode_tmap_bf16_3d(&tmV, p.v, VCH * 64, dp.bs_v, static_cast<uint64_t>(dp.nblk_v) * p.Hkv, 64,
+                             std::min(dp.bs_v, kStageKeys)))
+      return cudaErrorInvalidValue;
+  }
   auto kern = decode_split_kernel<ECH, VCH, NSTAGE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (e != cudaSuccess) return e;

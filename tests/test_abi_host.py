@@ -182,3 +182,18 @@ def test_binding_band_options():
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError):   # lengths must be CUDA int32
         sdpa.Band(seq_len_q=torch.zeros(2, dtype=torch.int32)).options()
+
+
+def test_decode_paged_rejects_bad_tables(lib):
+    shp = _shape(B=2, Hq=4, Hkv=2, L=1, S=100, E=64, Ev=64)
+
+    def call(pg):
+        return lib.sdpa_decode_paged(ctypes.byref(shp), None, pg, P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 1,
+                                     0, P(FAKE), P(FAKE), P(FAKE), 1 << 30, None)
+    assert call(None) == INVALID
+    good = dict(page_table_k=FAKE, page_table_v=FAKE, block_size_k=16, block_size_v=16, max_blocks=7,
+                num_blocks_k=20, num_blocks_v=20)
+    for bad in (dict(block_size_k=12), dict(block_size_v=4), dict(max_blocks=6), dict(page_table_k=FAKE + 2),
+                dict(page_table_v=None), dict(num_blocks_k=0)):
+        pg = sdpa.PagedKV(**{**good, **bad})
+        assert call(ctypes.byref(pg)) == INVALID, bad
