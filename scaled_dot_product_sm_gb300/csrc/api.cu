@@ -228,6 +228,8 @@ sdpa_status run_decode(const Checked& c, const Band& band, const void* q, const 
   dp.page_stride = paged ? paged->max_blocks : 0;
   dp.bs_k = paged ? paged->block_size_k : 0;
   dp.bs_v = paged ? paged->block_size_v : 0;
+  dp.lg_k = dp.bs_k ? __builtin_ctz(static_cast<unsigned>(dp.bs_k)) : 0;
+  dp.lg_v = dp.bs_v ? __builtin_ctz(static_cast<unsigned>(dp.bs_v)) : 0;
   dp.nblk_k = paged ? static_cast<int>(paged->num_blocks_k) : 0;
   dp.nblk_v = paged ? static_cast<int>(paged->num_blocks_v) : 0;
   return from_cuda(launch_decode(dp, st));

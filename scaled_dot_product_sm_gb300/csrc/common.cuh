@@ -106,6 +106,7 @@ struct DecodeParams {
   const int* page_v;
   int page_stride;       // entries per table row (>= ceil(S / bs))
   int bs_k, bs_v;        // keys per block, powers of two >= 8
+  int lg_k, lg_v;        // log2 of bs_k, bs_v
   int nblk_k, nblk_v;    // blocks in the containers
 };
 

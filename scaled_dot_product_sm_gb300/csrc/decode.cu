@@ -35,7 +35,7 @@ namespace {
 
 using namespace sdpa_ptx;
 
-constexpr int kStageKeys = 64;
+constexpr int kStageKeys = 64;   // the paged producer's shifts assume 64 = 2^6
 constexpr int kRowsPerCta = 8;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -105,42 +105,80 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      for (int it = 0; it < nst; ++it) {
-        const int s = it % NSTAGE;
-        mbar_wait(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, status_code(0x21));
-        uint8_t* st = smem + s * SM::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], SM::kStageBytes);
-        const int key0 = k_first + it * kStageKeys;
-        if (!dp.page_k) {
+    if (!dp.page_k) {
+      if (lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        for (int it = 0; it < nst; ++it) {
+          const int s = it % NSTAGE;
+          mbar_wait(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, status_code(0x21));
+          uint8_t* st = smem + s * SM::kStageBytes;
+          mbar_arrive_expect_tx(&full[s], SM::kStageBytes);
+          const int key0 = k_first + it * kStageKeys;
 #pragma unroll
           for (int c = 0; c < ECH; ++c) tma_load_3d(st + c * kStageKeys * 128, &tmK, &full[s], c * 64, key0, bk);
 #pragma unroll
           for (int c = 0; c < VCH; ++c)
             tma_load_3d(st + SM::kKBytes + c * kStageKeys * 128, &tmV, &full[s], c * 64, key0, bk);
-        } else {
-          // Paged: keys key0.. of this stage come from the container blocks the table names;
-          // a box covers min(bs, 64) keys and lands on a 1024-byte (8-row) boundary, so the
-          // 128-byte swizzle of the stage is the same as with one 64-row box.  An entry past
-          // the table or outside the container becomes block nblk: past the tensor map, so the
-          // copy fills zeros (those keys lie past the sequence's length and are masked).
-#pragma unroll 1
-          for (int kv = 0; kv < 2; ++kv) {
-            const int bs = kv ? dp.bs_v : dp.bs_k, nblk = kv ? dp.nblk_v : dp.nblk_k;
-            const int* table = (kv ? dp.page_v : dp.page_k) + static_cast<size_t>(b) * dp.page_stride;
-            const int rows_box = min(bs, kStageKeys), nch = kv ? VCH : ECH;
-            uint8_t* dst0 = st + (kv ? SM::kKBytes : 0);
-            for (int sub = 0; sub < kStageKeys / rows_box; ++sub) {
-              const int key = key0 + sub * rows_box, blk = key / bs;
-              int page = blk < dp.page_stride ? __ldg(table + blk) : nblk;
-              if (page < 0 || page >= nblk) page = nblk;
-              const int z = page * p.Hkv + hk;
-              for (int c = 0; c < nch; ++c)
-                tma_load_3d(dst0 + c * kStageKeys * 128 + sub * rows_box * 128, kv ? &tmV : &tmK, &full[s], c * 64,
-                            key & (bs - 1), z);
-            }
+        }
+      }
+    } else {
+      // Paged caches.  A stage's keys come from the container blocks the tables name, one
+      // box per min(bs, 64) keys; a box lands on a 1024-byte (8-row) boundary, so the stage's
+      // 128-byte swizzle is the same as with one 64-row box.  The warp reads the tables 32
+      // boxes at a time (lane l holds box w + l) and lane 0 takes each box's entry by a shuffle.
+      // An entry past the table or outside the container becomes block nblk: past the tensor
+      // map, so the copy fills zeros (those keys lie past the sequence's length and are masked).
+      if (lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+      }
+      const int rows_k = min(dp.bs_k, kStageKeys), rows_v = min(dp.bs_v, kStageKeys);
+      const int lgr_k = min(dp.lg_k, 6), lgr_v = min(dp.lg_v, 6);   // log2 of rows per box
+      const int* tab_k = dp.page_k + static_cast<size_t>(b) * dp.page_stride;
+      const int* tab_v = dp.page_v + static_cast<size_t>(b) * dp.page_stride;
+      // z coordinate (block * Hkv + head) of box i counted from key k_first
+      auto box_z = [&](const int* tab, int i, int lgr, int lg, int nblk) {
+        const int blk = (k_first + (i << lgr)) >> lg;
+        int page = blk < dp.page_stride ? __ldg(tab + blk) : -1;
+        if (page < 0 || page >= nblk) page = nblk;
+        return page * p.Hkv + hk;
+      };
+      int wk = 0, wv = 0;   // first box of the window each lane holds an entry of
+      int zk = box_z(tab_k, lane, lgr_k, dp.lg_k, dp.nblk_k), zv = box_z(tab_v, lane, lgr_v, dp.lg_v, dp.nblk_v);
+      for (int it = 0; it < nst; ++it) {
+        const int s = it % NSTAGE;
+        mbar_wait(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, status_code(0x21));
+        uint8_t* st = smem + s * SM::kStageBytes;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], SM::kStageBytes);
+        const int key0 = k_first + it * kStageKeys;
+        const int nbk = kStageKeys >> lgr_k, nbv = kStageKeys >> lgr_v;
+        for (int sub = 0; sub < nbk; ++sub) {
+          const int i = (it << (6 - lgr_k)) + sub;
+          if (i >= wk + 32) {
+            wk += 32;
+            zk = box_z(tab_k, wk + lane, lgr_k, dp.lg_k, dp.nblk_k);
+          }
+          const int z = __shfl_sync(0xffffffffu, zk, i - wk);
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < ECH; ++c)
+              tma_load_3d(st + c * kStageKeys * 128 + sub * rows_k * 128, &tmK, &full[s], c * 64,
+                          (key0 + sub * rows_k) & (dp.bs_k - 1), z);
+          }
+        }
+        for (int sub = 0; sub < nbv; ++sub) {
+          const int i = (it << (6 - lgr_v)) + sub;
+          if (i >= wv + 32) {
+            wv += 32;
+            zv = box_z(tab_v, wv + lane, lgr_v, dp.lg_v, dp.nblk_v);
+          }
+          const int z = __shfl_sync(0xffffffffu, zv, i - wv);
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < VCH; ++c)
+              tma_load_3d(st + SM::kKBytes + c * kStageKeys * 128 + sub * rows_v * 128, &tmV, &full[s], c * 64,
+                          (key0 + sub * rows_v) & (dp.bs_v - 1), z);
           }
         }
       }

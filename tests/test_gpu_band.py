@@ -125,7 +125,9 @@ def test_band_forward_routes_l1_to_decode():
 
 
 def test_plain_causal_equals_top_left_right_bound_zero():
-    """is_causal and the band {top_left, right_bound 0} give bit-identical results."""
+    """is_causal and the band {top_left, right_bound 0} give bit-identical O, LSE, dK and
+    dV (dQ is summed by bulk reductions whose order between key tiles is not fixed, so two
+    runs may differ in the last bits of dQ)."""
     q, k, v, dO, _ = random_inputs(1, 4, 2, 300, 300, 128, 128, torch.bfloat16, seed=220)
     qd, kd, vd, dOd = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
     o1, l1 = sdpa.sdpa_forward(qd, kd, vd, None, None, True, True)
@@ -134,5 +136,6 @@ def test_plain_causal_equals_top_left_right_bound_zero():
     g2 = sdpa.sdpa_backward(qd, kd, vd, o2, dOd, l2, None, None, False, True, band=sdpa.Band(right_bound=0))
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    for a, b in zip(g1, g2):
-        assert torch.equal(a, b)
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    d = (g1[0].float() - g2[0].float()).norm() / g1[0].float().norm()
+    assert d <= 1e-3, d
