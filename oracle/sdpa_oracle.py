@@ -36,6 +36,13 @@ Sources for each step (page title, section):
     Options (Padding mask, Diagonal masking options) and Scaled Dot Product
     Attention, Args (seq_len_q, seq_len_kv, diagonal_alignment,
     diagonal_band_left_bound, diagonal_band_right_bound);
+  * attention dropout: one uniform u per weight, keep where u >= p, kept
+    weights scaled by 1/(1-p): O = (P o m) V with m = keep / (1 - p); the
+    backward replays m: dV = (P o m)^T dO, dP = (dO V^T) o m, the softmax
+    VJP unchanged ("Scaled dot-product attention (forward and backward)",
+    section 2.5); the uniforms come from a Philox counter-based generator
+    with a seed and an offset ("Attention" (cuDNN), Configurable Options:
+    Dropout, Philox RNG dropout);
   * paged K/V caches: K_cache[b, h, s, d] = K_container[page_table_k[b, s / bs_k],
     h, s mod bs_k, d], likewise V, with containers (num_blocks, H, bs, D) and
     page tables (B, ceil(S / bs)): "Attention" (cuDNN), Configurable Options
@@ -44,6 +51,13 @@ Sources for each step (page title, section):
 Readings where the pages are silent (every one also listed in the design notes):
   * a fully blocked row has LSE = -inf, O = 0, dQ = 0 and contributes nothing
     to dK/dV; padded query rows (i >= seq_len_q[b]) are such rows;
+  * dropout uniforms (the pages fix the rule u >= p but not the generator's
+    layout): Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random
+    numbers: as easy as 1, 2, 3", SC 2011) with key (seed, 0) and counter
+    (j // 16, i, b * Hq + h, offset); its four 64-bit words give 16 uniforms
+    of 16 bits, word t // 4, bits 16 * (t % 4).. for key j = 16 * (j // 16) + t;
+    keep iff u16 >= ceil(p * 65536) (so the drop probability is p rounded up
+    to a multiple of 2^-16), scale 1 / (1 - p);
   * "row" and "column" of the band bounds are measured from the aligned
     diagonal (row i's diagonal column is i, or i + seq_len_kv - seq_len_q
     when bottom-right aligned), and the band, the padding, the additive mask
@@ -63,6 +77,7 @@ import numpy as np
 __all__ = [
     "default_scale", "ref_forward", "ref_backward", "ref_forward_rows",
     "ref_group", "causal_bias", "band_bias", "Band", "gather_paged", "ref_forward_paged",
+    "philox4x64_10", "dropout_keep", "Dropout",
 ]
 
 NEG_INF = -np.inf
@@ -132,6 +147,83 @@ def band_bias(L: int, S: int, band: "Band", b: int) -> np.ndarray:
     if band.left_bound is not None:
         visible &= j > diag - band.left_bound
     return np.where(visible, 0.0, NEG_INF)
+
+
+# ------------------------------------------------------------------ dropout
+_PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)   # round multipliers
+_PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)   # key increments (Weyl sequence)
+_M64 = (1 << 64) - 1
+
+
+def philox4x64_10(counter, key):
+    """Philox4x64 with 10 rounds on one 256-bit counter (Python integers, exact).
+
+    A round multiplies counter words 0 and 2 by the two multipliers (128-bit
+    products split into high and low halves), mixes the high halves with
+    words 1, 3 and the key, and bumps the key by the Weyl constants.
+    """
+    c = [int(x) & _M64 for x in counter]
+    k = [int(x) & _M64 for x in key]
+    for _ in range(10):
+        p0 = _PHILOX_M[0] * c[0]
+        p1 = _PHILOX_M[1] * c[2]
+        c = [(p1 >> 64) ^ c[1] ^ k[0], p1 & _M64, (p0 >> 64) ^ c[3] ^ k[1], p0 & _M64]
+        k = [(k[0] + _PHILOX_W[0]) & _M64, (k[1] + _PHILOX_W[1]) & _M64]
+    return c
+
+
+def _mulhilo64(a, m):
+    """(high, low) 64-bit halves of a * m for a uint64 array and a constant, via 32-bit limbs."""
+    a = a.astype(np.uint64)
+    lo32 = np.uint64(0xFFFFFFFF)
+    a0, a1 = a & lo32, a >> np.uint64(32)
+    m0, m1 = np.uint64(m & 0xFFFFFFFF), np.uint64(m >> 32)
+    p00, p01, p10, p11 = a0 * m0, a0 * m1, a1 * m0, a1 * m1
+    mid = (p00 >> np.uint64(32)) + (p01 & lo32) + (p10 & lo32)
+    lo = (p00 & lo32) | ((mid & lo32) << np.uint64(32))
+    hi = p11 + (p01 >> np.uint64(32)) + (p10 >> np.uint64(32)) + (mid >> np.uint64(32))
+    return hi, lo
+
+
+def _philox_arrays(c0, c1, c2, c3, k0, k1):
+    """philox4x64_10 applied elementwise to uint64 counter arrays (same arithmetic, vectorised)."""
+    c = [np.asarray(x, dtype=np.uint64) for x in (c0, c1, c2, c3)]
+    k = [np.uint64(k0 & _M64), np.uint64(k1 & _M64)]
+    with np.errstate(over="ignore"):
+        for _ in range(10):
+            hi0, lo0 = _mulhilo64(c[0], _PHILOX_M[0])
+            hi1, lo1 = _mulhilo64(c[2], _PHILOX_M[1])
+            c = [hi1 ^ c[1] ^ k[0], lo1, hi0 ^ c[3] ^ k[1], lo0]
+            k = [k[0] + np.uint64(_PHILOX_W[0]), k[1] + np.uint64(_PHILOX_W[1])]
+    return c
+
+
+class Dropout:
+    """Attention dropout of one call: probability p in [0, 1), 64-bit seed and offset."""
+
+    def __init__(self, p: float, seed: int, offset: int = 0):
+        if not (0.0 <= p < 1.0):
+            raise ValueError("dropout probability must be in [0, 1)")
+        self.p, self.seed, self.offset = float(p), int(seed) & _M64, int(offset) & _M64
+
+    def threshold16(self) -> int:
+        """Uniforms below this 16-bit value drop their weight: ceil(p * 2^16)."""
+        return int(math.ceil(self.p * 65536.0))
+
+
+def dropout_keep(dropout: "Dropout", bh: int, rows, S: int) -> np.ndarray:
+    """keep[r, j] for query rows `rows` of head bh (= b * Hq + h) and keys 0..S-1."""
+    rows = np.asarray(rows, dtype=np.int64)
+    ngroups = (S + 15) // 16
+    g = np.arange(ngroups, dtype=np.uint64)[None, :]
+    i = rows.astype(np.uint64)[:, None]
+    shape = (len(rows), ngroups)
+    w = _philox_arrays(np.broadcast_to(g, shape), np.broadcast_to(i, shape), np.full(shape, bh, np.uint64),
+                       np.full(shape, dropout.offset, np.uint64), dropout.seed, 0)
+    u16 = np.empty((len(rows), ngroups * 16), dtype=np.uint64)
+    for t in range(16):
+        u16[:, t::16] = (w[t // 4] >> np.uint64(16 * (t % 4))) & np.uint64(0xFFFF)
+    return u16[:, :S] >= np.uint64(dropout.threshold16())
 
 
 def _masked_softmax(s: np.ndarray, bias: np.ndarray):
@@ -225,17 +317,26 @@ def _alpha(scale, E):
     return float(scale)
 
 
-def _head_forward(q, k, v, bias, alpha):
+def _head_forward(q, k, v, bias, alpha, m=None):
+    """O = (P o m) V (m = None: no dropout), LSE and P (before dropout)."""
     P, lse = _masked_softmax(_scores(q, k, alpha), bias)
-    return P @ v, lse, P
+    return (P if m is None else P * m) @ v, lse, P
+
+
+def _dropout_m(dropout, b, h, Hq, L, S):
+    """m = keep / (1 - p) of head (b, h), or None without dropout (course chapter, section 2.5)."""
+    if dropout is None or dropout.p == 0.0:
+        return None
+    return dropout_keep(dropout, b * Hq + h, np.arange(L), S) / (1.0 - dropout.p)
 
 
 def ref_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                return_P=False, band=None):
+                return_P=False, band=None, dropout=None):
     """O [B,Hq,L,Ev] and LSE [B,Hq,L] of softmax(alpha*Q*K^T + mask + causal + band)*V.
 
     Query head h reads KV head h // (Hq // Hkv) (repeat_interleave).  band:
-    None or a Band (padding lengths, diagonal alignment and bounds).
+    None or a Band (padding lengths, diagonal alignment and bounds).  dropout:
+    None or a Dropout; P (returned on request) and LSE are before dropout.
     """
     q, k, v, mask = _as64(q), _as64(k), _as64(v), _as64(mask)
     B, Hq, Hkv, L, S, E, Ev = _check_shapes(q, k, v, mask, enable_gqa)
@@ -248,16 +349,20 @@ def ref_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=Fals
         for h in range(Hq):
             kv = h // G
             o, lse, P = _head_forward(q[b, h], k[b, kv], v[b, kv],
-                                      _head_bias(mask, b, h, L, S, is_causal, band), alpha)
+                                      _head_bias(mask, b, h, L, S, is_causal, band), alpha,
+                                      _dropout_m(dropout, b, h, Hq, L, S))
             O[b, h], LSE[b, h] = o, lse
             if return_P:
                 Ps[b, h] = P
     return (O, LSE, Ps) if return_P else (O, LSE)
 
 
-def _head_backward(q, k, v, P, o, dO, alpha):
-    dV = P.T @ dO
+def _head_backward(q, k, v, P, o, dO, alpha, m=None):
+    """dQ, dK, dV, D of one head; with dropout m: dV = (P o m)^T dO, dP = (dO V^T) o m."""
+    dV = (P if m is None else P * m).T @ dO
     dP = dO @ v.T
+    if m is not None:
+        dP = dP * m
     D = _row_D(P, dP)
     # the identity D_i = dO_i . O_i of section 2.3 must hold for the oracle's own P
     np.testing.assert_allclose(D, (dO * o).sum(axis=1), rtol=1e-9, atol=1e-9)
@@ -266,7 +371,7 @@ def _head_backward(q, k, v, P, o, dO, alpha):
 
 
 def ref_backward(q, k, v, dO, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                 return_D=False, band=None):
+                 return_D=False, band=None, dropout=None):
     """dQ [B,Hq,L,E], dK [B,Hkv,S,E], dV [B,Hkv,S,Ev] of L = sum(O * dO).
 
     dK and dV of a KV head are summed over the Hq/Hkv query heads that read it
@@ -285,8 +390,9 @@ def ref_backward(q, k, v, dO, mask=None, scale=None, is_causal=False, enable_gqa
         for h in range(Hq):
             kv = h // G
             bias = _head_bias(mask, b, h, L, S, is_causal, band)
-            o, _, P = _head_forward(q[b, h], k[b, kv], v[b, kv], bias, alpha)
-            dq, dk, dv, D = _head_backward(q[b, h], k[b, kv], v[b, kv], P, o, dO[b, h], alpha)
+            m = _dropout_m(dropout, b, h, Hq, L, S)
+            o, _, P = _head_forward(q[b, h], k[b, kv], v[b, kv], bias, alpha, m)
+            dq, dk, dv, D = _head_backward(q[b, h], k[b, kv], v[b, kv], P, o, dO[b, h], alpha, m)
             dQ[b, h] = dq
             dK[b, kv] += dk
             dV[b, kv] += dv
@@ -295,7 +401,7 @@ def ref_backward(q, k, v, dO, mask=None, scale=None, is_causal=False, enable_gqa
 
 
 def ref_forward_rows(q, k, v, b, h, rows, mask=None, scale=None, is_causal=False,
-                     enable_gqa=False, band=None):
+                     enable_gqa=False, band=None, dropout=None):
     """O and LSE of selected query rows of one (b, h): for sampled checks of large runs.
 
     Each row is an independent problem (course chapter, section 2.1: every
@@ -319,6 +425,8 @@ def ref_forward_rows(q, k, v, b, h, rows, mask=None, scale=None, is_causal=False
     if band is not None:
         bias = bias + band_bias(L, S, band, b)[rows]
     P, lse = _masked_softmax(_scores(qh, kh, alpha), bias)
+    if dropout is not None and dropout.p > 0.0:
+        P = P * (dropout_keep(dropout, b * q.shape[1] + h, rows, S) / (1.0 - dropout.p))
     return P @ vh, lse
 
 

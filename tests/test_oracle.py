@@ -338,8 +338,8 @@ def test_pin(pin):
 
 
 # --------------------------------------------------------------------------- mutants
-# The applicable pitfalls of section 5 (dropout mutants s07-s09 do not apply:
-# dropout is outside this library).
+# The pitfalls of section 5 without dropout; the dropout ones (s07-s09) are
+# planted in tests/test_oracle_dropout.py.
 
 def _m_scale_1_over_d(E):
     return 1.0 / E
