@@ -197,9 +197,23 @@ sdpa_status sdpa_decode_noalloc(const sdpa_shape* shape,
  *            are masked (a sliding window of left_bound keys ending at the
  *            diagonal).
  * All of it applies together with the additive mask; a row left without keys
- * follows the empty-row rule above.  The backward must get the forward's
- * options.  Other values of diagonal_alignment, or misaligned length
- * pointers, -> INVALID_ARG. */
+ * follows the empty-row rule above.
+ *
+ *  dropout_p, dropout_seed, dropout_offset  Attention dropout of the prefill
+ *            forward and backward ("Scaled dot-product attention (forward and
+ *            backward)", section 2.5; cuDNN "Attention", Philox RNG dropout):
+ *            o = (P o m) v with m = keep / (1 - p), one uniform per weight,
+ *            keep where u >= p; the backward replays m (dV = (P o m)^T dO,
+ *            dP = (dO v^T) o m).  lse stays the statistics of P before dropout.
+ *            Weight (b, h, i, j) takes its uniform from Philox4x64-10 with key
+ *            (dropout_seed, 0) and counter (j / 16, i, b * Hq + h,
+ *            dropout_offset): 16-bit chunk j % 16 of the 256-bit output (word
+ *            (j % 16) / 4, bits 16 * (j % 4)), kept iff >= ceil(p * 65536).
+ *            p = 0: no dropout; p outside [0, 1) -> INVALID_ARG.  The decode
+ *            entry points take no dropout (dropout_p != 0 -> INVALID_ARG).
+ *
+ * The backward must get the forward's options.  Other values of
+ * diagonal_alignment, or misaligned length pointers, -> INVALID_ARG. */
 typedef enum { SDPA_TOP_LEFT = 0, SDPA_BOTTOM_RIGHT = 1 } sdpa_diag_alignment;
 
 typedef struct {
@@ -208,6 +222,9 @@ typedef struct {
   int32_t diagonal_alignment;  /* sdpa_diag_alignment */
   int32_t right_bound;
   int32_t left_bound;
+  double dropout_p;
+  uint64_t dropout_seed;
+  uint64_t dropout_offset;
 } sdpa_options;
 
 /* sdpa_forward, sdpa_backward and sdpa_decode with sdpa_options in place of

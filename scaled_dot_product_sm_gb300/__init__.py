@@ -19,7 +19,8 @@ from .build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "SdpaError", "load_library", "exported_symbols", "sdpa_forward", "sdpa_backward", "sdpa_decode",
     "forward_workspace_bytes", "backward_workspace_bytes", "decode_workspace_bytes",
-    "decode_num_splits", "last_device_status", "Shape", "Options", "Band", "PagedKV", "sdpa_decode_paged",
+    "decode_num_splits", "last_device_status", "Shape", "Options", "Band", "Dropout", "PagedKV",
+    "sdpa_decode_paged",
     "build", "LIB_PATH",
 ]
 
@@ -52,7 +53,8 @@ class Options(ctypes.Structure):
     """sdpa_options: padding lengths (device int32 [B] or NULL), diagonal alignment, band bounds."""
     _fields_ = [("seq_len_q", ctypes.c_void_p), ("seq_len_kv", ctypes.c_void_p),
                 ("diagonal_alignment", ctypes.c_int32), ("right_bound", ctypes.c_int32),
-                ("left_bound", ctypes.c_int32)]
+                ("left_bound", ctypes.c_int32), ("dropout_p", ctypes.c_double), ("dropout_seed", ctypes.c_uint64),
+                ("dropout_offset", ctypes.c_uint64)]
 
 
 class Band:
@@ -67,7 +69,7 @@ class Band:
         self.seq_len_q, self.seq_len_kv = seq_len_q, seq_len_kv
         self.alignment, self.right_bound, self.left_bound = alignment, right_bound, left_bound
 
-    def options(self) -> Options:
+    def options(self, dropout=None) -> Options:
         import torch
         for t in (self.seq_len_q, self.seq_len_kv):
             if t is not None and (not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous()):
@@ -75,9 +77,18 @@ class Band:
         align = {"top_left": 0, "bottom_right": 1}.get(self.alignment)
         if align is None:
             raise ValueError("alignment is top_left or bottom_right")
+        dp, ds, do = (0.0, 0, 0) if dropout is None else (float(dropout.p), int(dropout.seed), int(dropout.offset))
         return Options(_ptr(self.seq_len_q), _ptr(self.seq_len_kv), align,
                        -1 if self.right_bound is None else int(self.right_bound),
-                       0 if self.left_bound is None else int(self.left_bound))
+                       0 if self.left_bound is None else int(self.left_bound), dp, ds & (2 ** 64 - 1),
+                       do & (2 ** 64 - 1))
+
+
+class Dropout:
+    """Attention dropout of a prefill forward/backward pair: probability p in [0, 1), 64-bit seed and offset."""
+
+    def __init__(self, p: float, seed: int, offset: int = 0):
+        self.p, self.seed, self.offset = float(p), int(seed), int(offset)
 
 
 class PagedKV(ctypes.Structure):
@@ -229,11 +240,12 @@ def decode_num_splits(q, k, v) -> int:
 
 
 def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                 out=None, lse=None, workspace=None, stream=None, band=None):
+                 out=None, lse=None, workspace=None, stream=None, band=None, dropout=None):
     """O [B,Hq,L,Ev] (dtype of q) and LSE [B,Hq,L] fp32 of softmax(scale*q k^T + mask) v.
 
     band: None, or a Band (padding lengths, diagonal alignment, bounds) used in
-    place of is_causal (sdpa_forward_opts).
+    place of is_causal (sdpa_forward_opts).  dropout: None or a Dropout (the
+    backward must get the same one).
     """
     import torch
     lib = load_library()
@@ -248,8 +260,10 @@ def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=Fal
     if workspace is None and need:
         workspace = _workspace(need, q.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if band is None and dropout is not None:
+        band = Band(right_bound=0 if is_causal else None)
     if band is not None:
-        opts = band.options()
+        opts = band.options(dropout)
         st = lib.sdpa_forward_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(mask),
                                    _scale(scale), int(bool(enable_gqa)), _ptr(out), _ptr(lse), _ptr(workspace), wsb,
                                    _stream(stream))
@@ -263,7 +277,7 @@ def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=Fal
 
 
 def sdpa_backward(q, k, v, o, dO, lse, mask=None, scale=None, is_causal=False, enable_gqa=False,
-                  dq=None, dk=None, dv=None, workspace=None, stream=None, band=None):
+                  dq=None, dk=None, dv=None, workspace=None, stream=None, band=None, dropout=None):
     """dQ, dK, dV of sum(O * dO); o and lse are the forward's outputs (same band)."""
     import torch
     lib = load_library()
@@ -275,8 +289,10 @@ def sdpa_backward(q, k, v, o, dO, lse, mask=None, scale=None, is_causal=False, e
     if workspace is None:
         workspace = _workspace(lib.sdpa_backward_workspace_bytes(ctypes.byref(shp)), q.device)
     wsb = workspace.numel() * workspace.element_size()
+    if band is None and dropout is not None:
+        band = Band(right_bound=0 if is_causal else None)
     if band is not None:
-        opts = band.options()
+        opts = band.options(dropout)
         st = lib.sdpa_backward_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                     _ptr(dO), _ptr(lse), _ptr(mask), _scale(scale), int(bool(enable_gqa)), _ptr(dq),
                                     _ptr(dk), _ptr(dv), _ptr(workspace), wsb, _stream(stream))

@@ -104,6 +104,23 @@ sdpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_
 // The band of the plain entry points: no padding, top-left, causal = right bound 0.
 Band plain_band(int is_causal) { return Band{nullptr, nullptr, 0, is_causal ? 0 : -1, 0}; }
 
+DropoutParams no_dropout() { return DropoutParams{0, 0u, 1.f, 0ull, 0ull}; }
+
+// Dropout of sdpa_options: p in [0, 1) (INVALID_ARG otherwise); p = 0 is no dropout.
+sdpa_status dropout_from_options(const sdpa_options* o, DropoutParams* d) {
+  *d = no_dropout();
+  if (!o) return SDPA_OK;
+  const double pr = o->dropout_p;
+  if (!(pr >= 0.0 && pr < 1.0)) return SDPA_ERR_INVALID_ARG;
+  if (pr == 0.0) return SDPA_OK;
+  d->active = 1;
+  d->thr16 = static_cast<unsigned>(std::ceil(pr * 65536.0));
+  d->scale = static_cast<float>(1.0 / (1.0 - pr));
+  d->seed = o->dropout_seed;
+  d->offset = o->dropout_offset;
+  return SDPA_OK;
+}
+
 // Checks sdpa_options and turns them into a Band (NULL options = no padding, no band).
 sdpa_status band_from_options(const sdpa_options* o, const Checked& c, Band* band) {
   *band = plain_band(0);
@@ -143,6 +160,7 @@ void fill_fwd(FwdParams& p, const Checked& c, const void* q, const void* k, cons
   p.scale = alpha;
   p.scale_log2 = alpha * kLog2e;
   p.band = band;
+  p.drop = no_dropout();
   p.status = status_ptr();
 }
 
@@ -303,10 +321,14 @@ sdpa_status forward_impl(const sdpa_shape* shape, const sdpa_options* opts, int 
   if ((s = check_io(c, q, k, v, mask, o, lse)) != SDPA_OK) return s;
   Band band = plain_band(is_causal);
   if (opts && (s = band_from_options(opts, c, &band)) != SDPA_OK) return s;
+  DropoutParams drop;
+  if ((s = dropout_from_options(opts, &drop)) != SDPA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (routes_to_decode(c)) return run_decode(c, band, q, k, v, mask, alpha, 0, o, lse, workspace, workspace_bytes, st);
+  if (routes_to_decode(c) && !drop.active)   // dropout is a training-time forward: the prefill kernels
+    return run_decode(c, band, q, k, v, mask, alpha, 0, o, lse, workspace, workspace_bytes, st);
   FwdParams p;
   fill_fwd(p, c, q, k, v, mask, alpha, band, o, lse);
+  p.drop = drop;
   if (c.bf16 && fwd_tc_supported(c.E, c.Ev)) {
     if ((c.L + 255) / 256 > 65535) return SDPA_ERR_UNSUPPORTED;
     return from_cuda(launch_fwd_tc(p, st));
@@ -344,6 +366,7 @@ sdpa_status decode_impl(const sdpa_shape* shape, const sdpa_options* opts, const
   if ((s = check_io(c, q, k, v, mask, o, lse)) != SDPA_OK) return s;
   Band band = plain_band(0);
   if (opts && (s = band_from_options(opts, c, &band)) != SDPA_OK) return s;
+  if (opts && opts->dropout_p != 0.0) return SDPA_ERR_INVALID_ARG;   // no dropout in the decode
   if (paged && (s = check_paged(paged, c)) != SDPA_OK) return s;
   if (!c.bf16 || !decode_supported(c.E, c.Ev)) return SDPA_ERR_UNSUPPORTED;
   const int want = num_splits > 0 ? num_splits : auto_splits(c);
@@ -374,6 +397,8 @@ sdpa_status backward_impl(const sdpa_shape* shape, const sdpa_options* opts, int
   if (mask && !aligned16(mask)) return SDPA_ERR_INVALID_ARG;
   Band band = plain_band(is_causal);
   if (opts && (s = band_from_options(opts, c, &band)) != SDPA_OK) return s;
+  DropoutParams drop;
+  if ((s = dropout_from_options(opts, &drop)) != SDPA_OK) return s;
   const size_t need = bwd_ws(c);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SDPA_ERR_INVALID_ARG;
   BwdParams p;
@@ -403,6 +428,7 @@ sdpa_status backward_impl(const sdpa_shape* shape, const sdpa_options* opts, int
   p.scale = alpha;
   p.scale_log2 = alpha * kLog2e;
   p.band = band;
+  p.drop = drop;
   p.status = status_ptr();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (p.dq_acc) {

@@ -92,8 +92,13 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
       const float p0 = expf(x[0] - msafe), p1 = expf(x[1] - msafe);
       l[rr] = l[rr] * corr + warp_sum(p0 + p1);
       m[rr] = mnew;
-      sP[r * kKT + lane] = p0;
-      sP[r * kKT + lane + 32] = p1;
+      float d0 = 1.f, d1 = 1.f;   // dropout keep flags: P o keep feeds P V (the row sum keeps every weight)
+      if (p.drop.active) {
+        d0 = dropout_m1(p.drop, i, j0 + lane, bh) != 0.f ? 1.f : 0.f;
+        d1 = dropout_m1(p.drop, i, j0 + lane + 32, bh) != 0.f ? 1.f : 0.f;
+      }
+      sP[r * kKT + lane] = p0 * d0;
+      sP[r * kKT + lane + 32] = p1 * d1;
 #pragma unroll
       for (int c = 0; c < kMaxC; ++c) acc[rr][c] *= corr;
     }
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
   for (int rr = 0; rr < 4; ++rr) {
     const int i = i0 + warp * 4 + rr;
     if (i >= L) continue;
-    const float inv = (l[rr] > 0.f) ? 1.f / l[rr] : 0.f;
+    const float inv = (l[rr] > 0.f) ? p.drop.scale / l[rr] : 0.f;   // 1/(1-p) applied once
     T* o = static_cast<T*>(p.o) + (static_cast<size_t>(bh) * L + i) * Ev;
 #pragma unroll
     for (int c = 0; c < kMaxC; ++c) {
@@ -208,6 +213,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
           s *= p.scale;
           if (mask) s += mask[static_cast<size_t>(i) * S + j];
           const float pij = expf(s - lse[rr]);
+          if (p.drop.active) dp *= dropout_m1(p.drop, i, j, bh);   // dP o m
           ds = pij * (dp - Dv[rr]);
         }
         sP[r * kKT + jj] = ds;
@@ -315,7 +321,14 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
             s *= p.scale;
             if (mask) s += mask[static_cast<size_t>(i) * S + j];
             pij = expf(s - sL[r]);
-            ds = pij * (dp - sD[r]);
+            if (p.drop.active) {   // dV takes P o m, dS takes (dP o m - D)
+              const float mij = dropout_m1(p.drop, i, j, b * p.Hq + h);
+              dp *= mij;
+              ds = pij * (dp - sD[r]);
+              pij *= mij;
+            } else {
+              ds = pij * (dp - sD[r]);
+            }
           }
           sP[kk * kQT + r] = pij;
           sS[kk * kQT + r] = ds;

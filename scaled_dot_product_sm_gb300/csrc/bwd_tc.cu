@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p) {
   }
 }
 
-template <int E_>
+template <int E_, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO, TcBwdArgs a) {
@@ -388,6 +388,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (qc + j < p.L) nl[j] = fmaf(__ldg(mcol + static_cast<size_t>(j) * p.S), kLog2e, nl[j]);
         }
       }
+      // dropout: keep bits of this lane's key for the warp's 32 queries (bit jj = query qc + jj).
+      // Lane l draws the 32 keys kw..kw+31 of query qc + l (two Philox blocks, the forward's
+      // layout), and 32 ballots transpose the bits so that lane j gets key kw + j's column.
+      uint32_t col = 0xFFFFFFFFu;
+      if (DROP) {
+        const unsigned kw = static_cast<unsigned>(k0 + wq * 32), bh = static_cast<unsigned>(b * p.Hq + h);
+        uint32_t k16a[8], k16b[8];
+        dropout_keep16(p.drop, kw >> 4, static_cast<unsigned>(qc + lane), bh, k16a);
+        dropout_keep16(p.drop, (kw >> 4) + 1, static_cast<unsigned>(qc + lane), bh, k16b);
+        uint32_t word = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          word |= (k16a[c] & 1u) << (2 * c) | ((k16a[c] >> 16) & 1u) << (2 * c + 1);
+          word |= (k16b[c] & 1u) << (16 + 2 * c) | ((k16b[c] >> 16) & 1u) << (17 + 2 * c);
+        }
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const uint32_t bal = __ballot_sync(0xffffffffu, (word >> t) & 1u);
+          if (t == lane) col = bal;
+        }
+      }
       mbar_wait(s_full, i & 1, abort_flag, p.status, status_code(0x39));
       tc_fence_after();
       float x[kHalf];
@@ -435,13 +456,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dp_free);
-#pragma unroll
-      for (int j = 0; j < kHalf; j += 2) {                // dS^T = P^T (dP^T - D)
-        float t0, t1;
-        add2(t0, t1, d[j], d[j + 1], nd[j], nd[j + 1]);
-        mul2(d[j], d[j + 1], x[j], x[j + 1], t0, t1);
-      }
       uint32_t pp[kHalf / 2], pd[kHalf / 2];
+      if (DROP) {
+        // dropout: dS^T = P^T (dP^T o m - D), dV takes (P o m)^T, m = keep / (1 - p)
+#pragma unroll
+        for (int j = 0; j < kHalf; ++j) {
+          const float mj = ((col >> j) & 1u) ? p.drop.scale : 0.f;
+          const float xm = x[j] * mj;
+          d[j] = x[j] * fmaf(d[j], mj, nd[j]);
+          x[j] = xm;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kHalf; j += 2) {                // dS^T = P^T (dP^T - D)
+          float t0, t1;
+          add2(t0, t1, d[j], d[j + 1], nd[j], nd[j + 1]);
+          mul2(d[j], d[j + 1], x[j], x[j + 1], t0, t1);
+        }
+      }
 #pragma unroll
       for (int c = 0; c < kHalf / 2; ++c) {
         pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
@@ -548,14 +580,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int E>
+template <int E, bool DROP>
 cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
   using C = BwdCfg<E>;
   TcBwdArgs a;
   a.p = p;
   a.Lpad = (p.L + BQ - 1) / BQ * BQ;
   a.rowstats = p.D;
-  auto kern = bwd_tc_kernel<E>;
+  auto kern = bwd_tc_kernel<E, DROP>;
   // The register split in the main kernel assumes the launch reserves exactly kRegsLaunch per thread.
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -590,7 +622,8 @@ bool bwd_tc_supported(int E_, int Ev_) { return E_ == Ev_ && (E_ == 64 || E_ == 
 int bwd_tc_row_pad() { return BQ; }
 
 cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st) {
-  return p.E == 64 ? run_bwd<64>(p, st) : run_bwd<128>(p, st);
+  if (p.drop.active) return p.E == 64 ? run_bwd<64, true>(p, st) : run_bwd<128, true>(p, st);
+  return p.E == 64 ? run_bwd<64, false>(p, st) : run_bwd<128, false>(p, st);
 }
 
 }  // namespace sdpa_impl

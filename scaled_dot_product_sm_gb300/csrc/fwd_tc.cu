@@ -429,6 +429,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l_run = l_run * corr + rs;
+        if (p.drop.active) {
+          // dropout: the row sum above keeps every weight; P V gets P o keep (1/(1-p) at the end)
+#pragma unroll
+          for (int g = 0; g < BN / 16; ++g) {
+            uint32_t keep[8];
+            dropout_keep16(p.drop, static_cast<unsigned>((kb >> 4) + g), static_cast<unsigned>(row),
+                           static_cast<unsigned>(u.bh), keep);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) pk[g * 8 + c] &= keep[c];
+          }
+        }
         if (j > ja) {
           // O_t holds PV_t(ja..j-1) (complete: the commit after S_t(j) covered it)
           if (__any_sync(0xffffffffu, need)) {
@@ -464,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&o_final[t], oc_cnt & 1, abort_flag, p.status, status_code(0x1a));
       ++oc_cnt;
       tc_fence_after();
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const float inv = (l_run > 0.f) ? p.drop.scale / l_run : 0.f;   // dropout's 1/(1-p) (1 without)
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(u.bh) * p.L + row) * C::Ev;
 #pragma unroll
       for (int c = 0; c < C::Ev / 32; ++c) {

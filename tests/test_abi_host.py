@@ -197,3 +197,14 @@ def test_decode_paged_rejects_bad_tables(lib):
                 dict(page_table_v=None), dict(num_blocks_k=0)):
         pg = sdpa.PagedKV(**{**good, **bad})
         assert call(ctypes.byref(pg)) == INVALID, bad
+
+
+def test_dropout_options_are_checked(lib):
+    shp = _shape()
+    for p in (-0.1, 1.0, float("nan")):
+        o = sdpa.Options(None, None, 0, 0, 0, p, 1, 0)
+        assert _fwd_opts(lib, shp, ctypes.byref(o)) == INVALID, p
+    dshp = _shape(L=1)
+    o = sdpa.Options(None, None, 1, 0, 0, 0.1, 1, 0)   # the decode takes no dropout
+    assert lib.sdpa_decode_opts(ctypes.byref(dshp), ctypes.byref(o), P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 0,
+                                0, P(FAKE), P(FAKE), P(FAKE), 1 << 30, None) == INVALID
