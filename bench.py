@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--workload", default=MAIN,
                     choices=["tiny_f32", "tiny_f32_causal", "mha_causal_e64", "gqa_causal_e128", "padded_mask_e128",
-                             "padded_seqlen_e128", "gqa_swa_e128"],
+                             "padded_seqlen_e128", "gqa_swa_e128", "gqa_causal_dropout_e128"],
                     help="prefill workload of the step (default: the GQA causal E=128 headline workload)")
     ap.add_argument("--phase", choices=["all", "fwd", "bwd", "decode"], default="all",
                     help="profiling aid: run only the forward loop, the backward loop or the decode leg")
@@ -236,6 +236,7 @@ def run_ours(args, ws, rank, local):
     q, k, v, dO = (t.to(dev) for t in host[:4])
     mask = host[4].to(dev) if m_h is not None else None
     spec = workloads.make_band(w, seed=0)
+    drop = sdpa.Dropout(w.dropout, 0, 0) if w.dropout > 0 else None
     band = None
     if spec is not None:
         lens = [None if spec[n] is None else torch.tensor(spec[n], dtype=torch.int32).pin_memory()
@@ -254,11 +255,11 @@ def run_ours(args, ws, rank, local):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def fwd():
-        sdpa.sdpa_forward(q, k, v, mask, scale, w.is_causal, w.enable_gqa, out=o, lse=lse, band=band)
+        sdpa.sdpa_forward(q, k, v, mask, scale, w.is_causal, w.enable_gqa, out=o, lse=lse, band=band, dropout=drop)
 
     def bwd():
         sdpa.sdpa_backward(q, k, v, o, dO, lse, mask, scale, w.is_causal, w.enable_gqa, dq=dq, dk=dk, dv=dv,
-                           workspace=bws, band=band)
+                           workspace=bws, band=band, dropout=drop)
 
     if args.phase == "decode":
         return run_decode_only(args, ws, local, dev, peaks)
@@ -480,7 +481,7 @@ def run_ours(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "S": w.S, "E": w.E,
                    "Ev": w.Ev, "causal": w.is_causal, "gqa": w.enable_gqa, "scale": w.scale,
-                   "mask": w.mask, "band": spec,
+                   "mask": w.mask, "band": spec, "dropout": w.dropout,
                    "flops": "visible (query, key) pairs x 4E / 10E" if spec is not None else
                             "4/10 x B*Hq*L*S*E, halved for causal",
                    "step": "forward (O, LSE) + backward (dQ, dK, dV)", "seed": 0,
@@ -544,13 +545,14 @@ def cpu_oracle_sample(w, seconds_target=15.0, steps=None):
     (qs, ks, vs, dOs, ms), sub, flops, spec = _oracle_head_sample(w)
     band = None if spec is None else oracle.Band(spec["seq_len_q"], spec["seq_len_kv"], spec["alignment"],
                                                  spec["right_bound"], spec["left_bound"])
+    drop = oracle.Dropout(w.dropout, 0, 0) if w.dropout > 0 else None   # batch 0, head 0: the same mask rows
     times = []
     n = 0
     t_start = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band)
-        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band)
+        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band, dropout=drop)
+        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band, dropout=drop)
         times.append(time.perf_counter() - t0)
         n += 1
         if steps is not None and n >= steps:

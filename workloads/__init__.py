@@ -53,6 +53,7 @@ class Workload:
     description: str = ""
     band: str = "none"      # "none", "seqlen" (lengths U{256..S} as seq_len_q = seq_len_kv) or "window"
     window: int = 0         # left bound of the "window" band (causal about the top-left diagonal)
+    dropout: float = 0.0    # attention dropout probability (seed 0, offset 0)
 
     @property
     def torch_dtype(self):
@@ -103,6 +104,10 @@ WORKLOADS = {
         "gqa_swa_e128", B=2, Hq=32, Hkv=8, L=4096, S=4096, E=128, Ev=128, dtype="bf16",
         is_causal=False, enable_gqa=True, scale=1.0 / math.sqrt(128), mask="none", phases=("fwd", "bwd"),
         description="GQA causal bf16 with a sliding window of 1024 keys", band="window", window=1024),
+    "gqa_causal_dropout_e128": Workload(
+        "gqa_causal_dropout_e128", B=2, Hq=32, Hkv=8, L=4096, S=4096, E=128, Ev=128, dtype="bf16",
+        is_causal=True, enable_gqa=True, scale=1.0 / math.sqrt(128), mask="none", phases=("fwd", "bwd"),
+        description="the GQA causal workload with attention dropout p = 0.1", dropout=0.1),
     "gqa_decode_s32k": Workload(
         "gqa_decode_s32k", B=16, Hq=32, Hkv=8, L=1, S=32768, E=128, Ev=128, dtype="bf16",
         is_causal=False, enable_gqa=True, scale=1.0 / math.sqrt(128), mask="none",
