@@ -298,7 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * BN;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
-    const float sc = p.scale_log2;
+    // alpha*log2(e), kept > 0 (alpha = 0 becomes the smallest normal float, which
+    // gives the same exponentials): then the row max of the raw scores, scaled,
+    // is the max of the scaled scores, and x = s*sc - m is one FMA (unmasked path)
+    const float sc = fmaxf(p.scale_log2, 1.17549435e-38f);
     uint32_t sc_cnt = 0, oc_cnt = 0;       // s_full / o_final completions consumed
     for (int ur = 0;; ++ur) {
       const int k = unit_index(ur);
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld128(tS, v);
 #pragma unroll
           for (int i = 0; i < BN; i += 2)
-            mul2(x[i], x[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sc, sc);
+            x[i] = __uint_as_float(v[i]), x[i + 1] = __uint_as_float(v[i + 1]);   // raw scores
         }
         if (!(kb >= full_lo && kb + BN - 1 <= full_hi)) {   // warp-uniform: the tile crosses a boundary
           // this row sees key kb + i exactly for i in [ilo, ihi]
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u8 = 0; u8 < 8; ++u8) mx8[u8] = max3f(mx8[u8], x[i + u8], x[i + 8 + u8]);
         const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
                                fmaxf(mx8[6], mx8[7]));
-        const float m_new = fmaxf(m_run, mx);
+        const float m_new = fmaxf(m_run, MASKED ? mx : mx * sc);
         const bool need = m_new > m_run + kRescaleThreshold;
         const float m_use = need ? m_new : m_run;
         const float nm = (m_use == kNegInf) ? 0.f : -m_use;
@@ -420,7 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < BN; i += 2) {
           float a0, a1;
-          add2(a0, a1, x[i], x[i + 1], nm, nm);
+          if (MASKED)
+            add2(a0, a1, x[i], x[i + 1], nm, nm);        // x already scaled (and the mask added)
+          else
+            fma2(a0, a1, x[i], x[i + 1], sc, sc, nm, nm);  // s*sc - m
           a0 = ex2(a0);
           a1 = ex2(a1);
           const int q4 = (i >> 1) & 3;

@@ -212,3 +212,10 @@ def test_forward_routes_l1_to_decode():
     ref_o, ref_lse = oracle.ref_forward(q, k, v)
     o, lse = sdpa.sdpa_forward(q.cuda(), k.cuda(), v.cuda())
     check_forward(o, lse, ref_o, ref_lse, True)
+
+
+@pytest.mark.parametrize("causal,mask_kind", [(True, "none"), (False, "bias")])
+def test_bf16_zero_scale(causal, mask_kind):
+    """alpha = 0: every open key gets the same weight (the mean of the open values)."""
+    run_case(1, 4, 2, 200, 260, 128, 128, torch.bfloat16, causal, mask_kind, (1, 1) if mask_kind != "none" else None,
+             1 if mask_kind != "none" else 0, scale=0.0, seed=31)
