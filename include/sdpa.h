@@ -205,11 +205,12 @@ sdpa_status sdpa_decode_noalloc(const sdpa_shape* shape,
  *            o = (P o m) v with m = keep / (1 - p), one uniform per weight,
  *            keep where u >= p; the backward replays m (dV = (P o m)^T dO,
  *            dP = (dO v^T) o m).  lse stays the statistics of P before dropout.
- *            Weight (b, h, i, j) takes its uniform from Philox4x64-10 with key
- *            (dropout_seed, 0) and counter (j / 16, i, b * Hq + h,
- *            dropout_offset): 16-bit chunk j % 16 of the 256-bit output (word
- *            (j % 16) / 4, bits 16 * (j % 4)), kept iff >= ceil(p * 65536).
- *            p = 0: no dropout; p outside [0, 1) -> INVALID_ARG.  The decode
+ *            Weight (b, h, i, j) takes its uniform from Philox4x32-10 with key
+ *            (dropout_seed mod 2^32, dropout_seed / 2^32) and counter (j / 8, i,
+ *            b * Hq + h, dropout_offset): 16-bit chunk j % 8 of the 128-bit
+ *            output (word (j % 8) / 2, bits 16 * (j % 2)), kept iff
+ *            >= ceil(p * 65536).  p = 0: no dropout; p outside [0, 1), or
+ *            dropout_offset >= 2^32 with p != 0 -> INVALID_ARG.  The decode
  *            entry points take no dropout (dropout_p != 0 -> INVALID_ARG).
  *
  * The backward must get the forward's options.  Other values of

@@ -51,13 +51,14 @@ Sources for each step (page title, section):
 Readings where the pages are silent (every one also listed in the design notes):
   * a fully blocked row has LSE = -inf, O = 0, dQ = 0 and contributes nothing
     to dK/dV; padded query rows (i >= seq_len_q[b]) are such rows;
-  * dropout uniforms (the pages fix the rule u >= p but not the generator's
-    layout): Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random
-    numbers: as easy as 1, 2, 3", SC 2011) with key (seed, 0) and counter
-    (j // 16, i, b * Hq + h, offset); its four 64-bit words give 16 uniforms
-    of 16 bits, word t // 4, bits 16 * (t % 4).. for key j = 16 * (j // 16) + t;
-    keep iff u16 >= ceil(p * 65536) (so the drop probability is p rounded up
-    to a multiple of 2^-16), scale 1 / (1 - p);
+  * dropout uniforms (the pages fix the rule u >= p and name a Philox
+    generator with a seed and an offset, not its width or layout):
+    Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers:
+    as easy as 1, 2, 3", SC 2011) with key (seed mod 2^32, seed // 2^32) and
+    counter (j // 8, i, b * Hq + h, offset), offset < 2^32; its four 32-bit
+    words give 8 uniforms of 16 bits, word t // 2, bits 16 * (t % 2).. for key
+    j = 8 * (j // 8) + t; keep iff u16 >= ceil(p * 65536) (so the drop
+    probability is p rounded up to a multiple of 2^-16), scale 1 / (1 - p);
   * "row" and "column" of the band bounds are measured from the aligned
     diagonal (row i's diagonal column is i, or i + seq_len_kv - seq_len_q
     when bottom-right aligned), and the band, the padding, the additive mask
@@ -77,7 +78,7 @@ import numpy as np
 __all__ = [
     "default_scale", "ref_forward", "ref_backward", "ref_forward_rows",
     "ref_group", "causal_bias", "band_bias", "Band", "gather_paged", "ref_forward_paged",
-    "philox4x64_10", "dropout_keep", "Dropout",
+    "philox4x32_10", "dropout_keep", "Dropout",
 ]
 
 NEG_INF = -np.inf
@@ -150,61 +151,52 @@ def band_bias(L: int, S: int, band: "Band", b: int) -> np.ndarray:
 
 
 # ------------------------------------------------------------------ dropout
-_PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)   # round multipliers
-_PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)   # key increments (Weyl sequence)
+_PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # round multipliers
+_PHILOX_W = (0x9E3779B9, 0xBB67AE85)   # key increments (Weyl sequence)
+_M32 = (1 << 32) - 1
 _M64 = (1 << 64) - 1
 
 
-def philox4x64_10(counter, key):
-    """Philox4x64 with 10 rounds on one 256-bit counter (Python integers, exact).
+def philox4x32_10(counter, key):
+    """Philox4x32 with 10 rounds on one 128-bit counter (Python integers, exact).
 
-    A round multiplies counter words 0 and 2 by the two multipliers (128-bit
+    A round multiplies counter words 0 and 2 by the two multipliers (64-bit
     products split into high and low halves), mixes the high halves with
     words 1, 3 and the key, and bumps the key by the Weyl constants.
     """
-    c = [int(x) & _M64 for x in counter]
-    k = [int(x) & _M64 for x in key]
+    c = [int(x) & _M32 for x in counter]
+    k = [int(x) & _M32 for x in key]
     for _ in range(10):
         p0 = _PHILOX_M[0] * c[0]
         p1 = _PHILOX_M[1] * c[2]
-        c = [(p1 >> 64) ^ c[1] ^ k[0], p1 & _M64, (p0 >> 64) ^ c[3] ^ k[1], p0 & _M64]
-        k = [(k[0] + _PHILOX_W[0]) & _M64, (k[1] + _PHILOX_W[1]) & _M64]
+        c = [(p1 >> 32) ^ c[1] ^ k[0], p1 & _M32, (p0 >> 32) ^ c[3] ^ k[1], p0 & _M32]
+        k = [(k[0] + _PHILOX_W[0]) & _M32, (k[1] + _PHILOX_W[1]) & _M32]
     return c
 
 
-def _mulhilo64(a, m):
-    """(high, low) 64-bit halves of a * m for a uint64 array and a constant, via 32-bit limbs."""
-    a = a.astype(np.uint64)
-    lo32 = np.uint64(0xFFFFFFFF)
-    a0, a1 = a & lo32, a >> np.uint64(32)
-    m0, m1 = np.uint64(m & 0xFFFFFFFF), np.uint64(m >> 32)
-    p00, p01, p10, p11 = a0 * m0, a0 * m1, a1 * m0, a1 * m1
-    mid = (p00 >> np.uint64(32)) + (p01 & lo32) + (p10 & lo32)
-    lo = (p00 & lo32) | ((mid & lo32) << np.uint64(32))
-    hi = p11 + (p01 >> np.uint64(32)) + (p10 >> np.uint64(32)) + (mid >> np.uint64(32))
-    return hi, lo
-
-
 def _philox_arrays(c0, c1, c2, c3, k0, k1):
-    """philox4x64_10 applied elementwise to uint64 counter arrays (same arithmetic, vectorised)."""
-    c = [np.asarray(x, dtype=np.uint64) for x in (c0, c1, c2, c3)]
-    k = [np.uint64(k0 & _M64), np.uint64(k1 & _M64)]
-    with np.errstate(over="ignore"):
-        for _ in range(10):
-            hi0, lo0 = _mulhilo64(c[0], _PHILOX_M[0])
-            hi1, lo1 = _mulhilo64(c[2], _PHILOX_M[1])
-            c = [hi1 ^ c[1] ^ k[0], lo1, hi0 ^ c[3] ^ k[1], lo0]
-            k = [k[0] + np.uint64(_PHILOX_W[0]), k[1] + np.uint64(_PHILOX_W[1])]
+    """philox4x32_10 applied elementwise to counter arrays (same arithmetic, vectorised:
+    a 32 x 32-bit product is exact in uint64)."""
+    m32 = np.uint64(_M32)
+    c = [np.asarray(x, dtype=np.uint64) & m32 for x in (c0, c1, c2, c3)]
+    k = [np.uint64(k0 & _M32), np.uint64(k1 & _M32)]
+    for _ in range(10):
+        p0 = c[0] * np.uint64(_PHILOX_M[0])
+        p1 = c[2] * np.uint64(_PHILOX_M[1])
+        c = [(p1 >> np.uint64(32)) ^ c[1] ^ k[0], p1 & m32, (p0 >> np.uint64(32)) ^ c[3] ^ k[1], p0 & m32]
+        k = [(k[0] + np.uint64(_PHILOX_W[0])) & m32, (k[1] + np.uint64(_PHILOX_W[1])) & m32]
     return c
 
 
 class Dropout:
-    """Attention dropout of one call: probability p in [0, 1), 64-bit seed and offset."""
+    """Attention dropout of one call: probability p in [0, 1), 64-bit seed, 32-bit offset."""
 
     def __init__(self, p: float, seed: int, offset: int = 0):
         if not (0.0 <= p < 1.0):
             raise ValueError("dropout probability must be in [0, 1)")
-        self.p, self.seed, self.offset = float(p), int(seed) & _M64, int(offset) & _M64
+        if not (0 <= int(offset) <= _M32):
+            raise ValueError("dropout offset must be in [0, 2^32)")
+        self.p, self.seed, self.offset = float(p), int(seed) & _M64, int(offset)
 
     def threshold16(self) -> int:
         """Uniforms below this 16-bit value drop their weight: ceil(p * 2^16)."""
@@ -214,15 +206,15 @@ class Dropout:
 def dropout_keep(dropout: "Dropout", bh: int, rows, S: int) -> np.ndarray:
     """keep[r, j] for query rows `rows` of head bh (= b * Hq + h) and keys 0..S-1."""
     rows = np.asarray(rows, dtype=np.int64)
-    ngroups = (S + 15) // 16
+    ngroups = (S + 7) // 8
     g = np.arange(ngroups, dtype=np.uint64)[None, :]
     i = rows.astype(np.uint64)[:, None]
     shape = (len(rows), ngroups)
     w = _philox_arrays(np.broadcast_to(g, shape), np.broadcast_to(i, shape), np.full(shape, bh, np.uint64),
-                       np.full(shape, dropout.offset, np.uint64), dropout.seed, 0)
-    u16 = np.empty((len(rows), ngroups * 16), dtype=np.uint64)
-    for t in range(16):
-        u16[:, t::16] = (w[t // 4] >> np.uint64(16 * (t % 4))) & np.uint64(0xFFFF)
+                       np.full(shape, dropout.offset, np.uint64), dropout.seed & _M32, dropout.seed >> 32)
+    u16 = np.empty((len(rows), ngroups * 8), dtype=np.uint64)
+    for t in range(8):
+        u16[:, t::8] = (w[t // 2] >> np.uint64(16 * (t % 2))) & np.uint64(0xFFFF)
     return u16[:, :S] >= np.uint64(dropout.threshold16())
 
 

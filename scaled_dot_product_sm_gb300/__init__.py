@@ -85,7 +85,8 @@ class Band:
 
 
 class Dropout:
-    """Attention dropout of a prefill forward/backward pair: probability p in [0, 1), 64-bit seed and offset."""
+    """Attention dropout of a prefill forward/backward pair: probability p in [0, 1), 64-bit seed, offset in
+    [0, 2^32) (the library checks both and answers INVALID_ARG)."""
 
     def __init__(self, p: float, seed: int, offset: int = 0):
         self.p, self.seed, self.offset = float(p), int(seed), int(offset)

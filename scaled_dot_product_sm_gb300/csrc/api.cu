@@ -104,20 +104,23 @@ sdpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_
 // The band of the plain entry points: no padding, top-left, causal = right bound 0.
 Band plain_band(int is_causal) { return Band{nullptr, nullptr, 0, is_causal ? 0 : -1, 0}; }
 
-DropoutParams no_dropout() { return DropoutParams{0, 0u, 1.f, 0ull, 0ull}; }
+DropoutParams no_dropout() { return DropoutParams{0, 0u, 1.f, 0u, 0u, 0u}; }
 
-// Dropout of sdpa_options: p in [0, 1) (INVALID_ARG otherwise); p = 0 is no dropout.
+// Dropout of sdpa_options: p in [0, 1) and an offset below 2^32 (INVALID_ARG
+// otherwise: the offset fills one 32-bit counter word); p = 0 is no dropout.
 sdpa_status dropout_from_options(const sdpa_options* o, DropoutParams* d) {
   *d = no_dropout();
   if (!o) return SDPA_OK;
   const double pr = o->dropout_p;
   if (!(pr >= 0.0 && pr < 1.0)) return SDPA_ERR_INVALID_ARG;
   if (pr == 0.0) return SDPA_OK;
+  if (o->dropout_offset > 0xFFFFFFFFull) return SDPA_ERR_INVALID_ARG;
   d->active = 1;
   d->thr16 = static_cast<unsigned>(std::ceil(pr * 65536.0));
   d->scale = static_cast<float>(1.0 / (1.0 - pr));
-  d->seed = o->dropout_seed;
-  d->offset = o->dropout_offset;
+  d->seed_lo = static_cast<unsigned>(o->dropout_seed & 0xFFFFFFFFull);
+  d->seed_hi = static_cast<unsigned>(o->dropout_seed >> 32);
+  d->offset = static_cast<unsigned>(o->dropout_offset);
   return SDPA_OK;
 }
 

@@ -389,19 +389,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // dropout: keep bits of this lane's key for the warp's 32 queries (bit jj = query qc + jj).
-      // Lane l draws the 32 keys kw..kw+31 of query qc + l (two Philox blocks, the forward's
+      // Lane l draws the 32 keys kw..kw+31 of query qc + l (four Philox blocks, the forward's
       // layout), and 32 ballots transpose the bits so that lane j gets key kw + j's column.
       uint32_t col = 0xFFFFFFFFu;
       if (DROP) {
         const unsigned kw = static_cast<unsigned>(k0 + wq * 32), bh = static_cast<unsigned>(b * p.Hq + h);
-        uint32_t k16a[8], k16b[8];
-        dropout_keep16(p.drop, kw >> 4, static_cast<unsigned>(qc + lane), bh, k16a);
-        dropout_keep16(p.drop, (kw >> 4) + 1, static_cast<unsigned>(qc + lane), bh, k16b);
         uint32_t word = 0;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          word |= (k16a[c] & 1u) << (2 * c) | ((k16a[c] >> 16) & 1u) << (2 * c + 1);
-          word |= (k16b[c] & 1u) << (16 + 2 * c) | ((k16b[c] >> 16) & 1u) << (17 + 2 * c);
+        for (int g = 0; g < 4; ++g) {
+          uint32_t k8[4];
+          dropout_keep8(p.drop, (kw >> 3) + g, static_cast<unsigned>(qc + lane), bh, k8);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            word |= (k8[c] & 1u) << (8 * g + 2 * c) | ((k8[c] >> 16) & 1u) << (8 * g + 2 * c + 1);
         }
 #pragma unroll
         for (int t = 0; t < 32; ++t) {

@@ -61,30 +61,29 @@ __device__ __forceinline__ BandRows band_rows(const Band& bd, int b, int L, int 
 // section 2.5: one uniform per weight, keep where u >= p, kept weights scaled by
 // 1/(1-p), the backward replaying the mask; "Attention" (cuDNN), Philox RNG
 // dropout with a seed and an offset).  Weight (b, h, i, j) takes its uniform from
-// Philox4x64-10 with key (seed, 0) and counter (j / 16, i, b * Hq + h, offset):
-// the four 64-bit words give sixteen 16-bit uniforms, word t / 4, bits
-// 16 * (t % 4) .. for key j = 16 * (j / 16) + t.  keep iff u16 >= thr16 =
-// ceil(p * 2^16) (thr16 = 65536 drops everything).
+// Philox4x32-10 with key (seed mod 2^32, seed / 2^32) and counter (j / 8, i,
+// b * Hq + h, offset): the four 32-bit words give eight 16-bit uniforms, word
+// t / 2, bits 16 * (t % 2) .. for key j = 8 * (j / 8) + t.  keep iff u16 >=
+// thr16 = ceil(p * 2^16) (thr16 = 65536 drops everything).
 struct DropoutParams {
   int active;            // 0: no dropout
   unsigned thr16;        // 0 .. 65536
   float scale;           // 1 / (1 - p)
-  unsigned long long seed, offset;
+  unsigned seed_lo, seed_hi, offset;
 };
 
-// Philox4x64 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random
 // numbers: as easy as 1, 2, 3", SC 2011): each round multiplies counter words 0
 // and 2 by fixed odd multipliers, mixes the high product halves with words 1 and
 // 3 and the key, and advances the key by two Weyl constants.
-__device__ __forceinline__ void philox4x64_10(unsigned long long c0, unsigned long long c1, unsigned long long c2,
-                                              unsigned long long c3, unsigned long long k0, unsigned long long k1,
-                                              unsigned long long (&w)[4]) {
-  constexpr unsigned long long kM0 = 0xD2E7470EE14C6C93ull, kM1 = 0xCA5A826395121157ull;
-  constexpr unsigned long long kW0 = 0x9E3779B97F4A7C15ull, kW1 = 0xBB67AE8584CAA73Bull;
+__device__ __forceinline__ void philox4x32_10(unsigned c0, unsigned c1, unsigned c2, unsigned c3, unsigned k0,
+                                              unsigned k1, uint32_t (&w)[4]) {
+  constexpr unsigned kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr unsigned kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const unsigned long long hi0 = __umul64hi(c0, kM0), lo0 = c0 * kM0;
-    const unsigned long long hi1 = __umul64hi(c2, kM1), lo1 = c2 * kM1;
+    const unsigned hi0 = __umulhi(c0, kM0), lo0 = c0 * kM0;
+    const unsigned hi1 = __umulhi(c2, kM1), lo1 = c2 * kM1;
     c0 = hi1 ^ c1 ^ k0;
     c1 = lo1;
     c2 = hi0 ^ c3 ^ k1;
@@ -98,26 +97,23 @@ __device__ __forceinline__ void philox4x64_10(unsigned long long c0, unsigned lo
   w[3] = c3;
 }
 
-// keep flags of the 16 keys 16g .. 16g+15 of query i, head bh, as 8 words of two
-// 16-bit lanes (0xFFFF = keep): word c covers keys 16g + 2c (low) and 16g + 2c + 1.
-__device__ __forceinline__ void dropout_keep16(const DropoutParams& d, unsigned g, unsigned i, unsigned bh,
-                                               uint32_t (&keep)[8]) {
-  unsigned long long w[4];
-  philox4x64_10(g, i, bh, d.offset, d.seed, 0ull, w);
+// keep flags of the 8 keys 8g .. 8g+7 of query i, head bh, as 4 words of two
+// 16-bit lanes (0xFFFF = keep): word c covers keys 8g + 2c (low) and 8g + 2c + 1.
+__device__ __forceinline__ void dropout_keep8(const DropoutParams& d, unsigned g, unsigned i, unsigned bh,
+                                              uint32_t (&keep)[4]) {
+  uint32_t w[4];
+  philox4x32_10(g, i, bh, d.offset, d.seed_lo, d.seed_hi, w);
   const unsigned thr = d.thr16 > 0xFFFFu ? 0u : d.thr16 * 0x10001u;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t u2 = static_cast<uint32_t>(w[c >> 1] >> (32 * (c & 1)));
-    keep[c] = d.thr16 > 0xFFFFu ? 0u : __vcmpgeu2(u2, thr);
-  }
+  for (int c = 0; c < 4; ++c) keep[c] = d.thr16 > 0xFFFFu ? 0u : __vcmpgeu2(w[c], thr);
 }
 
 // dropout multiplier m = keep / (1 - p) of one weight (query i, key j, head bh)
 __device__ __forceinline__ float dropout_m1(const DropoutParams& d, unsigned i, unsigned j, unsigned bh) {
-  unsigned long long w[4];
-  philox4x64_10(j >> 4, i, bh, d.offset, d.seed, 0ull, w);
-  const unsigned t = j & 15u;
-  const unsigned u = static_cast<unsigned>(w[t >> 2] >> (16 * (t & 3u))) & 0xFFFFu;
+  uint32_t w[4];
+  philox4x32_10(j >> 3, i, bh, d.offset, d.seed_lo, d.seed_hi, w);
+  const unsigned t = j & 7u;
+  const unsigned u = (w[t >> 1] >> (16 * (t & 1u))) & 0xFFFFu;
   return (d.thr16 <= 0xFFFFu && u >= d.thr16) ? d.scale : 0.f;
 }
 

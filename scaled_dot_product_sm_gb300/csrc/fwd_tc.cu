@@ -438,12 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.drop.active) {
           // dropout: the row sum above keeps every weight; P V gets P o keep (1/(1-p) at the end)
 #pragma unroll
-          for (int g = 0; g < BN / 16; ++g) {
-            uint32_t keep[8];
-            dropout_keep16(p.drop, static_cast<unsigned>((kb >> 4) + g), static_cast<unsigned>(row),
-                           static_cast<unsigned>(u.bh), keep);
+          for (int g = 0; g < BN / 8; ++g) {
+            uint32_t keep[4];
+            dropout_keep8(p.drop, static_cast<unsigned>((kb >> 3) + g), static_cast<unsigned>(row),
+                          static_cast<unsigned>(u.bh), keep);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) pk[g * 8 + c] &= keep[c];
+            for (int c = 0; c < 4; ++c) pk[g * 4 + c] &= keep[c];
           }
         }
         if (j > ja) {

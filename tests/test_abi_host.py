@@ -204,6 +204,8 @@ def test_dropout_options_are_checked(lib):
     for p in (-0.1, 1.0, float("nan")):
         o = sdpa.Options(None, None, 0, 0, 0, p, 1, 0)
         assert _fwd_opts(lib, shp, ctypes.byref(o)) == INVALID, p
+    o = sdpa.Options(None, None, 0, 0, 0, 0.1, 1, 1 << 32)   # the offset fills one 32-bit counter word
+    assert _fwd_opts(lib, shp, ctypes.byref(o)) == INVALID
     dshp = _shape(L=1)
     o = sdpa.Options(None, None, 1, 0, 0, 0.1, 1, 0)   # the decode takes no dropout
     assert lib.sdpa_decode_opts(ctypes.byref(dshp), ctypes.byref(o), P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 0,

@@ -1,5 +1,5 @@
 """GPU parity of attention dropout (course chapter section 2.5; cuDNN Philox RNG
-dropout) against the float64 oracle with the same Philox4x64-10 mask.
+dropout) against the float64 oracle with the same Philox4x32-10 mask.
 
 The mask itself is compared bit for bit (an integer decision): with V = I the
 output row is P o keep / (1 - p), so its zero pattern is the dropped set.  The

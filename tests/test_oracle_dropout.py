@@ -2,14 +2,20 @@
 attention (forward and backward)", section 2.5; cuDNN "Attention", Philox RNG
 dropout).
 
-The generator is pinned against numpy's own Philox (4x64, 10 rounds: an
-independent library implementation), the vectorised path against the scalar
-one, the mask layout against the documented counter rule; the dropout math by
+The generator (Philox4x32-10) is pinned against Triton's own Philox run by its
+CPU interpreter (an independent library implementation of the same function),
+the vectorised path against the scalar one, the mask layout against the
+documented counter rule; the dropout math by
 p = 0 reducing to the plain oracle, the kept fraction, unbiasedness over
 seeds, and central differences with the mask replayed.  The chapter's three
 dropout pitfalls (s07: dV ignores the mask, s08: dP ignores it, s09: keeping
 u < p) are planted and each is caught.
 """
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -18,45 +24,73 @@ import oracle
 from oracle import sdpa_oracle as so
 from workloads import random_inputs
 
-M64 = (1 << 64) - 1
+M32 = (1 << 32) - 1
+
+# Triton's Philox (triton.language.philox: 32-bit counter words, key = the 64-bit seed's
+# low and high halves, 10 rounds) evaluated by Triton's CPU interpreter in a child process.
+_TRITON_PHILOX = r"""
+import json, os, sys
+os.environ["TRITON_INTERPRET"] = "1"
+import torch, triton, triton.language as tl
+
+@triton.jit
+def _philox_kernel(out, c0p, c1p, c2p, c3p, seed, N: tl.constexpr):
+    n = tl.arange(0, N)
+    r0, r1, r2, r3 = tl.philox(seed, tl.load(c0p + n), tl.load(c1p + n), tl.load(c2p + n), tl.load(c3p + n), 10)
+    tl.store(out + 4 * n, r0)
+    tl.store(out + 4 * n + 1, r1)
+    tl.store(out + 4 * n + 2, r2)
+    tl.store(out + 4 * n + 3, r3)
+
+res = []
+for ctrs, seed in json.loads(sys.stdin.read()):
+    cols = [torch.tensor([c[w] for c in ctrs], dtype=torch.int64).to(torch.uint32) for w in range(4)]
+    out = torch.zeros(4 * len(ctrs), dtype=torch.uint32)
+    _philox_kernel[(1,)](out, *cols, seed, N=len(ctrs))
+    res.append([int(x) & 0xFFFFFFFF for x in out.to(torch.int64)])
+print(json.dumps(res))
+"""
 
 
 def _np(x):
     return None if x is None else x.to(torch.float64).numpy()
 
 
-def pin_philox_matches_numpy():
+def pin_philox_matches_triton():
+    pytest.importorskip("triton")
     rng = np.random.default_rng(5)
-    cases = [([1, 0, 0, 0], [0, 0]), ([0, 1, 0, 0], [123, 456]), ([7, 3, 99, 2 ** 63 + 5], [2 ** 64 - 1, 17])]
-    cases += [([int(x) for x in rng.integers(1, 2 ** 63, 4)], [int(x) for x in rng.integers(0, 2 ** 63, 2)])
-              for _ in range(4)]
-    for ctr, key in cases:
-        # numpy's Philox advances its 256-bit counter before each block: start one below
-        n = sum(c << (64 * i) for i, c in enumerate(ctr)) - 1
-        start = np.array([(n >> (64 * i)) & M64 for i in range(4)], dtype=np.uint64)
-        bg = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=start)
-        assert [int(x) for x in bg.random_raw(4)] == oracle.philox4x64_10(ctr, key)
+    ctrs = [[0, 0, 0, 0], [1, 0, 0, 0], [0, 1, 2, 3], [M32, M32, M32, M32], [7, 3, 99, 2 ** 31 + 5]]
+    ctrs += [[int(x) for x in rng.integers(0, 2 ** 32, 4)] for _ in range(3)]
+    seeds = [0, 123456789, 2 ** 40 + 7, 2 ** 63 + 12345]
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    got = subprocess.run([sys.executable, "-c", _TRITON_PHILOX], input=json.dumps([[ctrs, sd] for sd in seeds]),
+                         capture_output=True, text=True, env=env, timeout=300, check=True)
+    words = json.loads(got.stdout.strip().splitlines()[-1])
+    for sd, w in zip(seeds, words):
+        for n, ctr in enumerate(ctrs):
+            assert w[4 * n:4 * n + 4] == oracle.philox4x32_10(ctr, [sd & M32, sd >> 32]), (ctr, sd)
 
 
 def pin_vectorised_philox_matches_scalar():
     rng = np.random.default_rng(6)
-    c = rng.integers(0, 2 ** 63, (4, 64), dtype=np.int64).astype(np.uint64)
-    c[0, :3] = [0, 2 ** 64 - 1, 2 ** 63]
-    k0, k1 = 0xFEDCBA9876543210, 42
+    c = rng.integers(0, 2 ** 32, (4, 64), dtype=np.int64).astype(np.uint64)
+    c[0, :3] = [0, M32, 2 ** 31]
+    k0, k1 = 0xFEDCBA98, 42
     w = so._philox_arrays(c[0], c[1], c[2], c[3], k0, k1)
     for n in range(c.shape[1]):
-        assert [int(w[t][n]) for t in range(4)] == oracle.philox4x64_10([int(x) for x in c[:, n]], [k0, k1])
+        assert [int(w[t][n]) for t in range(4)] == oracle.philox4x32_10([int(x) for x in c[:, n]], [k0, k1])
 
 
 def pin_mask_layout():
-    """keep(i, j) of head bh: 16-bit chunk j % 16 of Philox((j // 16, i, bh, offset), (seed, 0)) >= ceil(p 2^16)."""
-    d = oracle.Dropout(0.37, seed=2 ** 40 + 7, offset=12345)
+    """keep(i, j) of head bh: 16-bit chunk j % 8 of Philox((j // 8, i, bh, offset), seed) >= ceil(p 2^16)."""
+    seed = 2 ** 40 + 7
+    d = oracle.Dropout(0.37, seed=seed, offset=12345)
     keep = oracle.dropout_keep(d, 5, [0, 3, 17], 40)
     thr = int(np.ceil(0.37 * 65536))
     for r, i in enumerate([0, 3, 17]):
         for j in range(40):
-            words = oracle.philox4x64_10([j // 16, i, 5, 12345], [2 ** 40 + 7, 0])
-            u = (words[(j % 16) // 4] >> (16 * (j % 4))) & 0xFFFF
+            words = oracle.philox4x32_10([j // 8, i, 5, 12345], [seed & M32, seed >> 32])
+            u = (words[(j % 8) // 2] >> (16 * (j % 2))) & 0xFFFF
             assert keep[r, j] == (u >= thr)
 
 
@@ -129,7 +163,7 @@ def pin_identity_values_show_the_mask():
     np.testing.assert_allclose(O[0, 0], np.where(keep, P[0, 0] / 0.7, 0.0), atol=1e-15)
 
 
-DROPOUT_PINS = [pin_philox_matches_numpy, pin_vectorised_philox_matches_scalar, pin_mask_layout, pin_p_zero_is_plain,
+DROPOUT_PINS = [pin_philox_matches_triton, pin_vectorised_philox_matches_scalar, pin_mask_layout, pin_p_zero_is_plain,
                 pin_keep_fraction, pin_unbiased_over_seeds, pin_dropout_gradcheck, pin_identity_values_show_the_mask]
 
 
@@ -177,7 +211,10 @@ def test_dropout_mutants_are_caught(name, monkeypatch):
     assert failed, f"dropout mutant {name} survived every pin"
 
 
-def test_dropout_rejects_bad_probability():
+def test_dropout_rejects_bad_probability_and_offset():
     for p in (-0.1, 1.0, 1.5):
         with pytest.raises(ValueError):
             oracle.Dropout(p, seed=0)
+    for off in (-1, 2 ** 32):
+        with pytest.raises(ValueError):
+            oracle.Dropout(0.1, seed=0, offset=off)
