@@ -270,8 +270,10 @@ int num_sms() {
   return g_sms[d];
 }
 
-bool encode_tmap_bf16_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
-                         uint32_t box1) {
+namespace {
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+bool encode_3d(void* tmap, CUtensorMapDataType dt, const void* base, const cuuint64_t (&dims)[3],
+               const cuuint64_t (&strides)[2], uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode_tried) {
@@ -285,15 +287,29 @@ bool encode_tmap_bf16_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1,
     }
   }
   if (!g_encode) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
   cuuint32_t box[3] = {box0, box1, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(tmap), dt, 3, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool encode_tmap_bf16_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                         uint32_t box1) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  return encode_3d(tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box0, box1,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool encode_tmap_f32_3d_plain(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                              uint32_t box1) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  return encode_3d(tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims, strides, box0, box1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace sdpa_impl

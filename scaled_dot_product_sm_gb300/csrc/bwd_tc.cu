@@ -60,7 +60,6 @@ using namespace sdpa_ptx;
 constexpr int BKV = 128;       // keys per CTA
 constexpr int BQ = 64;         // queries per iteration
 constexpr int kThreads = 512;
-constexpr int kNSQ = 3;        // query-tile stages (prefetch two tiles ahead)
 constexpr float kNegInf = -__builtin_huge_valf();
 
 constexpr int kRegsLaunch = 128;
@@ -73,19 +72,23 @@ constexpr int kHalf = BQ / 2;   // query columns per elementwise warp
 // The dQ^T MMA always runs with M = 128: at E = 64 its A rows 64..127 read the
 // 64-dim block after K (the start of V), and the drain never reads those rows of
 // dQ^T, so they cannot reach the result.
-template <int E_>
+template <int E_, bool MSTAGE>
 struct BwdCfg {
   static constexpr int E = E_, Ev = E_;
   static constexpr int ECH = E / 64;                          // 64-element column blocks
+  // query-tile stages (prefetch two tiles ahead; one when the mask tile takes the room at E = 128)
+  static constexpr int NSQ = (E == 128 && MSTAGE) ? 2 : 3;
   static constexpr int kKBytes = ECH * BKV * 128;             // K tile: ECH blocks of [128 keys x 64 dims]
   static constexpr int kQTile = ECH * BQ * 128;               // Q (or dO) tile: ECH blocks of [64 rows x 64 dims]
   static constexpr int kStage = 2 * kQTile + 1024;            // Q, dO, rowstats (512 B, padded)
+  static constexpr int kMaskBytes = MSTAGE ? BQ * BKV * 4 : 0;   // additive mask [64 queries x 128 keys] fp32
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKBytes;
   static constexpr int kOffStage = kOffV + kKBytes;
-  static constexpr int kOffDS = kOffStage + kNSQ * kStage;    // dS^T [128 keys x 64 queries] bf16
+  static constexpr int kOffDS = kOffStage + NSQ * kStage;     // dS^T [128 keys x 64 queries] bf16
   static constexpr int kOffDQ = kOffDS + BKV * 128;           // dQ staging [64 queries x E] fp32
-  static constexpr int kOffBar = kOffDQ + BQ * E * 4;
+  static constexpr int kOffMask = kOffDQ + BQ * E * 4;        // mask tile (TMA, one iteration ahead)
+  static constexpr int kOffBar = kOffMask + kMaskBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static_assert(E == 64 || E == 128, "head width");
 };
@@ -115,6 +118,7 @@ struct TcBwdArgs {
   BwdParams p;
   const float* rowstats;   // per (head, 64-row query tile): 64 x (-lse*log2e), then 64 x (-D)
   int Lpad;
+  int mslice_b, mslice_h;  // staged mask: [L, S] slice of (b, h) = b * mslice_b + h * mslice_h
 };
 
 template <int E>
@@ -171,11 +175,13 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p) {
   }
 }
 
-template <int E_, bool DROP>
+template <int E_, bool DROP, bool MSTAGE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO, TcBwdArgs a) {
-  using C = BwdCfg<E_>;
+                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                  const __grid_constant__ CUtensorMap tmM, TcBwdArgs a) {
+  using C = BwdCfg<E_, MSTAGE>;
+  constexpr int kNSQ = C::NSQ;
   constexpr int E = C::E, Ev = C::Ev, ECH = C::ECH;
   constexpr int kKBytes = C::kKBytes, kQTile = C::kQTile, kStage = C::kStage;
   constexpr int kOffK = C::kOffK, kOffV = C::kOffV, kOffStage = C::kOffStage, kOffDS = C::kOffDS,
@@ -196,7 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_full = p_free + 1;          // 1
   uint64_t* dq_free = dq_full + 1;         // 1
   uint64_t* kdv_done = dq_free + 1;        // 1
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kdv_done + 1);
+  uint64_t* m_full = kdv_done + 1;         // 1: staged mask tile landed
+  uint64_t* m_empty = m_full + 1;          // 1: mask tile read by the elementwise warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(m_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -247,6 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);    // one arrival per drain warp
     mbar_init(kdv_done, 1);
+    mbar_init(m_full, 1);
+    mbar_init(m_empty, 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -267,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmdO);
+      if (MSTAGE) prefetch_tmap(&tmM);
       mbar_arrive_expect_tx(kv_full, 2 * kKBytes);
       for (int c = 0; c < ECH; ++c) {
         tma_load_3d(smem + kOffK + c * BKV * 128, &tmK, kv_full, c * 64, k0, bkv);
@@ -286,6 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bulk_load(st + 2 * kQTile, a.rowstats + (static_cast<size_t>(bh) * a.Lpad + qt * BQ) * 2, BQ * 8,
                   &q_full[s]);
+        if (MSTAGE) {   // mask rows qt*BQ.., keys k0.. of head (b, h); zero-filled past L and S
+          mbar_wait(m_empty, (i & 1) ^ 1, abort_flag, p.status, status_code(0x3e));
+          mbar_arrive_expect_tx(m_full, C::kMaskBytes);
+          tma_load_3d(smem + C::kOffMask, &tmM, m_full, k0, qt * BQ,
+                      b * a.mslice_b + (hkv * p.G + g) * a.mslice_h);
+        }
       }
     } else if ((warp == 13 || warp == 14) && lane == 0 && n > 0) {
       // ---------------------------------------------------------- MMA issuers
@@ -380,7 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 v4 = reinterpret_cast<const float4*>(rs + hf * kHalf)[c];
         nl[4 * c] = v4.x, nl[4 * c + 1] = v4.y, nl[4 * c + 2] = v4.z, nl[4 * c + 3] = v4.w;
       }
-      if (p.mask) {
+      if (MSTAGE) {   // the staged tile: row = query, 128 keys per row; lanes read consecutive words
+        mbar_wait(m_full, i & 1, abort_flag, p.status, status_code(0x3f));
+        const float* mt = reinterpret_cast<const float*>(smem + C::kOffMask) + hf * kHalf * BKV + r;
+#pragma unroll
+        for (int j = 0; j < kHalf; ++j) nl[j] = fmaf(mt[j * BKV], kLog2e, nl[j]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m_empty);
+      } else if (p.mask) {
         if (key < p.S) {   // lanes are consecutive keys: each load instruction reads 128 contiguous bytes
           const float* mcol = p.mask + b * p.mask_sb + h * p.mask_sh + static_cast<size_t>(qc) * p.S + key;
 #pragma unroll
@@ -580,14 +604,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int E, bool DROP>
+template <int E, bool DROP, bool MSTAGE>
 cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
-  using C = BwdCfg<E>;
+  using C = BwdCfg<E, MSTAGE>;
   TcBwdArgs a;
   a.p = p;
   a.Lpad = (p.L + BQ - 1) / BQ * BQ;
   a.rowstats = p.D;
-  auto kern = bwd_tc_kernel<E, DROP>;
+  const long long LS = static_cast<long long>(p.L) * p.S;
+  a.mslice_b = static_cast<int>(p.mask_sb / LS);
+  a.mslice_h = static_cast<int>(p.mask_sh / LS);
+  auto kern = bwd_tc_kernel<E, DROP, MSTAGE>;
   // The register split in the main kernel assumes the launch reserves exactly kRegsLaunch per thread.
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -603,16 +630,28 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
       !encode_tmap_bf16_3d(&tmQ, p.q, E, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BQ) ||
       !encode_tmap_bf16_3d(&tmdO, p.dO, E, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BQ))
     return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap tmM = tmK;   // unused unless the mask is staged
+  if (MSTAGE) {
+    // the mask's distinct [L, S] slices: B x mask heads, or the heads alone, or one
+    const long long slices = a.mslice_b ? static_cast<long long>(p.B) * a.mslice_b : (a.mslice_h ? p.Hq : 1);
+    if (!encode_tmap_f32_3d_plain(&tmM, p.mask, p.S, p.L, static_cast<uint64_t>(slices), BKV, BQ))
+      return cudaErrorInvalidValue;
+  }
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) != cudaSuccess)
     return e;
   const unsigned groups = static_cast<unsigned>(p.B * p.Hkv), ktiles = static_cast<unsigned>((p.S + BKV - 1) / BKV);
   const dim3 grid = p.band.right >= 0 ? dim3(groups, ktiles) : dim3(ktiles, groups);
-  kern<<<grid, kThreads, C::kSmemBytes, st>>>(tmK, tmV, tmQ, tmdO, a);
+  kern<<<grid, kThreads, C::kSmemBytes, st>>>(tmK, tmV, tmQ, tmdO, tmM, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;
   const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n8 + 255) / 256, 152 * 16));
   bwd_dq_convert_kernel<E><<<blocks, 256, 0, st>>>(p);
   return cudaGetLastError();
+}
+
+template <bool DROP, bool MSTAGE>
+cudaError_t run_widths(const BwdParams& p, cudaStream_t st) {
+  return p.E == 64 ? run_bwd<64, DROP, MSTAGE>(p, st) : run_bwd<128, DROP, MSTAGE>(p, st);
 }
 
 }  // namespace
@@ -622,8 +661,12 @@ bool bwd_tc_supported(int E_, int Ev_) { return E_ == Ev_ && (E_ == 64 || E_ == 
 int bwd_tc_row_pad() { return BQ; }
 
 cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t st) {
-  if (p.drop.active) return p.E == 64 ? run_bwd<64, true>(p, st) : run_bwd<128, true>(p, st);
-  return p.E == 64 ? run_bwd<64, false>(p, st) : run_bwd<128, false>(p, st);
+  // An additive mask (16-byte aligned base, checked at the boundary) is staged
+  // through shared memory by TMA when its rows are 16-byte multiples (S a
+  // multiple of 4); otherwise the elementwise warps read it directly.
+  const bool mstage = p.mask && (p.S & 3) == 0;
+  if (p.drop.active) return mstage ? run_widths<true, true>(p, st) : run_widths<true, false>(p, st);
+  return mstage ? run_widths<false, true>(p, st) : run_widths<false, false>(p, st);
 }
 
 }  // namespace sdpa_impl

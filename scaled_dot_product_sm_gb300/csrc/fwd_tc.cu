@@ -74,7 +74,7 @@ struct FwdCfg {
   static_assert(NS >= 2, "the K/V ring needs two stages");
 };
 
-template <int ECH, int VCH, bool MASKED>
+template <int ECH, int VCH, bool MASKED, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, FwdParams p) {
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l_run = l_run * corr + rs;
-        if (p.drop.active) {
+        if (DROP) {
           // dropout: the row sum above keeps every weight; P V gets P o keep (1/(1-p) at the end)
 #pragma unroll
           for (int g = 0; g < BN / 8; ++g) {
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int ECH, int VCH, bool MASKED>
+template <int ECH, int VCH, bool MASKED, bool DROP>
 cudaError_t run(const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<ECH, VCH>;
   alignas(64) CUtensorMap tmQ, tmK, tmV;
@@ -520,7 +520,7 @@ cudaError_t run(const FwdParams& p, cudaStream_t st) {
       !encode_tmap_bf16_3d(&tmK, p.k, C::E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BN) ||
       !encode_tmap_bf16_3d(&tmV, p.v, C::Ev, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BN))
     return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<ECH, VCH, MASKED>;
+  auto kern = fwd_tc_kernel<ECH, VCH, MASKED, DROP>;
   // The register split in the kernel assumes the launch reserves exactly kRegsLaunch per thread.
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -537,13 +537,13 @@ cudaError_t run(const FwdParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <bool MASKED>
+template <bool MASKED, bool DROP>
 cudaError_t launch_widths(const FwdParams& p, cudaStream_t st) {
   const int ech = p.E / 64, vch = p.Ev / 64;
-  if (ech == 2 && vch == 2) return run<2, 2, MASKED>(p, st);
-  if (ech == 1 && vch == 1) return run<1, 1, MASKED>(p, st);
-  if (ech == 2 && vch == 1) return run<2, 1, MASKED>(p, st);
-  return run<1, 2, MASKED>(p, st);
+  if (ech == 2 && vch == 2) return run<2, 2, MASKED, DROP>(p, st);
+  if (ech == 1 && vch == 1) return run<1, 1, MASKED, DROP>(p, st);
+  if (ech == 2 && vch == 1) return run<2, 1, MASKED, DROP>(p, st);
+  return run<1, 2, MASKED, DROP>(p, st);
 }
 
 }  // namespace
@@ -551,7 +551,8 @@ cudaError_t launch_widths(const FwdParams& p, cudaStream_t st) {
 bool fwd_tc_supported(int E, int Ev) { return (E == 64 || E == 128) && (Ev == 64 || Ev == 128); }
 
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t st) {
-  return p.mask ? launch_widths<true>(p, st) : launch_widths<false>(p, st);
+  if (p.drop.active) return p.mask ? launch_widths<true, true>(p, st) : launch_widths<false, true>(p, st);
+  return p.mask ? launch_widths<true, false>(p, st) : launch_widths<false, false>(p, st);
 }
 
 }  // namespace sdpa_impl

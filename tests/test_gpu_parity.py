@@ -162,6 +162,10 @@ BF16_CASES = [
     (1, 8, 2, 100, 300, 128, 128, True, "none", None, 0),   # key tiles past every query: dK = dV = 0
     (2, 4, 1, 333, 333, 128, 128, True, "bias", (2, 4), 2), # GQA causal + per-head mask, ragged
     (1, 2, 2, 64, 1000, 128, 128, False, "block", (1, 2), 0),
+    # rows of a multiple of 4 keys: the backward stages the mask through shared memory
+    (2, 4, 2, 190, 512, 64, 64, False, "bias", (2, 4), 2),
+    (2, 4, 4, 257, 388, 128, 128, True, "bias", (2, 4), 1),
+    (3, 2, 1, 100, 132, 128, 128, False, "block", (3, 1), 1),
     # more work units than SMs: the persistent forward walks several units per CTA
     (2, 96, 32, 300, 333, 128, 128, True, "bias", (2, 1), 2),
     (1, 200, 200, 130, 140, 64, 64, False, "none", None, 0),
@@ -219,3 +223,4 @@ def test_bf16_zero_scale(causal, mask_kind):
     """alpha = 0: every open key gets the same weight (the mean of the open values)."""
     run_case(1, 4, 2, 200, 260, 128, 128, torch.bfloat16, causal, mask_kind, (1, 1) if mask_kind != "none" else None,
              1 if mask_kind != "none" else 0, scale=0.0, seed=31)
+
