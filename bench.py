@@ -365,7 +365,7 @@ def run_ours(args, ws, rank, local):
         roof = {"kernel": "fwd_tc_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": (traffic_for("fwd_tc_kernel", ["fwd_tc.cu", "ptx.cuh", "common.cuh"])
+                "traffic": (traffic_for("fwd_tc_kernel", ["fwd_tc_kernel.cuh", "ptx.cuh", "common.cuh"])
                             if w.name == MAIN else None),
                 "peak_source": f"{peak_src} bf16 dense burst",
                 "algorithmic_per_launch": f_fwd}

@@ -304,12 +304,12 @@ bool encode_tmap_bf16_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool encode_tmap_f32_3d_plain(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
-                              uint32_t box1) {
+bool encode_tmap_f32_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                        uint32_t box1, bool swizzle128) {
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
   return encode_3d(tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims, strides, box0, box1,
-                   CU_TENSOR_MAP_SWIZZLE_NONE);
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace sdpa_impl

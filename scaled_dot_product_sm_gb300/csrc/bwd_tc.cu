@@ -402,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* mt = reinterpret_cast<const float*>(smem + C::kOffMask) + hf * kHalf * BKV + r;
 #pragma unroll
         for (int j = 0; j < kHalf; ++j) nl[j] = fmaf(mt[j * BKV], kLog2e, nl[j]);
+        // the next fill is a TMA (async-proxy) write: order this lane's reads before it
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(m_empty);
       } else if (p.mask) {
@@ -634,7 +636,7 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
   if (MSTAGE) {
     // the mask's distinct [L, S] slices: B x mask heads, or the heads alone, or one
     const long long slices = a.mslice_b ? static_cast<long long>(p.B) * a.mslice_b : (a.mslice_h ? p.Hq : 1);
-    if (!encode_tmap_f32_3d_plain(&tmM, p.mask, p.S, p.L, static_cast<uint64_t>(slices), BKV, BQ))
+    if (!encode_tmap_f32_3d(&tmM, p.mask, p.S, p.L, static_cast<uint64_t>(slices), BKV, BQ, false))
       return cudaErrorInvalidValue;
   }
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) != cudaSuccess)

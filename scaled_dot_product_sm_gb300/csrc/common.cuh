@@ -215,10 +215,12 @@ cudaError_t decode_static_scratch(void** ptr, size_t* bytes);
 // Tensor-map encoder obtained from the driver at run time (no libcuda link).
 bool encode_tmap_bf16_3d(void* tmap /* CUtensorMap* */, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                          uint32_t box0, uint32_t box1);
-// The same for a dense fp32 [d2][d1][d0] array without swizzle (rows of box0 * 4 bytes
-// land back to back in shared memory); d0 * 4 must be a multiple of 16.
-bool encode_tmap_f32_3d_plain(void* tmap /* CUtensorMap* */, const void* base, uint64_t d0, uint64_t d1,
-                              uint64_t d2, uint32_t box0, uint32_t box1);
+// The same for a dense fp32 [d2][d1][d0] array; d0 * 4 must be a multiple of 16.
+// Without swizzle the box's rows (box0 * 4 bytes) land back to back in shared
+// memory; with the 128-byte swizzle box0 must be 32 (one 128-byte row) and the
+// 16-byte chunk c of row y lands at chunk c ^ (y % 8).
+bool encode_tmap_f32_3d(void* tmap /* CUtensorMap* */, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                        uint32_t box0, uint32_t box1, bool swizzle128);
 int num_sms();
 
 }  // namespace sdpa_impl

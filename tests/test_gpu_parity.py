@@ -224,3 +224,22 @@ def test_bf16_zero_scale(causal, mask_kind):
     run_case(1, 4, 2, 200, 260, 128, 128, torch.bfloat16, causal, mask_kind, (1, 1) if mask_kind != "none" else None,
              1 if mask_kind != "none" else 0, scale=0.0, seed=31)
 
+
+
+def test_masked_runs_are_bit_identical():
+    """The staged additive mask is recycled between TMA fills and the softmax / elementwise
+    warps' reads; a missing order between the two shows as run-to-run differences.  O, LSE,
+    dK and dV of repeated calls must match bit for bit (dQ is summed in a varying order)."""
+    B, Hq, Hkv, L, S, E = 4, 8, 8, 1024, 1024, 128
+    q, k, v, dO, mask = random_inputs(B, Hq, Hkv, L, S, E, E, torch.bfloat16, seed=51, mask_kind="bias",
+                                      mask_shape=(B, 1), full_rows=2)
+    qd, kd, vd, dOd, md = q.cuda(), k.cuda(), v.cuda(), dO.cuda(), mask.cuda()
+    o0, l0 = sdpa.sdpa_forward(qd, kd, vd, md)
+    g0 = sdpa.sdpa_backward(qd, kd, vd, o0, dOd, l0, md)
+    for _ in range(3):
+        o1, l1 = sdpa.sdpa_forward(qd, kd, vd, md)
+        g1 = sdpa.sdpa_backward(qd, kd, vd, o0, dOd, l0, md)
+        torch.cuda.synchronize()
+        assert torch.equal(o0, o1) and torch.equal(l0, l1)
+        assert torch.equal(g0[1], g1[1]) and torch.equal(g0[2], g1[2])
+    assert sdpa.last_device_status() == 0
