@@ -197,9 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_free = s_full + 1;           // 1
   uint64_t* dp_full = s_free + 1;          // 1
   uint64_t* dp_free = dp_full + 1;         // 1
-  uint64_t* p_full = dp_free + 1;          // 1
-  uint64_t* p_free = p_full + 1;           // 1
-  uint64_t* dq_full = p_free + 1;          // 1
+  uint64_t* pt_full = dp_free + 1;         // 1: P^T(i) in TMEM (one arrival per elementwise warp)
+  uint64_t* pt_free = pt_full + 1;         // 1: dV(i) complete (P^T columns free)
+  uint64_t* ds_full = pt_free + 1;         // 1: dS^T(i) in TMEM and shared memory
+  uint64_t* ds_free = ds_full + 1;         // 1: dK(i) and dQ^T(i) complete (dS^T buffers free)
+  uint64_t* dq_full = ds_free + 1;         // 1
   uint64_t* dq_free = dq_full + 1;         // 1
   uint64_t* kdv_done = dq_free + 1;        // 1
   uint64_t* m_full = kdv_done + 1;         // 1: staged mask tile landed
@@ -250,8 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(s_free, 8);     // one arrival per elementwise warp
     mbar_init(dp_full, 1);
     mbar_init(dp_free, 8);
-    mbar_init(p_full, 8);
-    mbar_init(p_free, 1);
+    mbar_init(pt_full, 8);
+    mbar_init(pt_free, 1);
+    mbar_init(ds_full, 8);
+    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);    // one arrival per drain warp
     mbar_init(kdv_done, 1);
@@ -350,14 +354,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n; ++i) {               // gradient MMAs
           const int s = i % kNSQ;
           const SmemDesc q_mn = dQ_mn + s * kStage, do_mn = q_mn + kQTile;
-          mbar_wait(p_full, i & 1, abort_flag, p.status, status_code(0x36));
+          // dV += P^T dO as soon as P^T is in TMEM (the elementwise warps are still on dS)
+          mbar_wait(pt_full, i & 1, abort_flag, p.status, status_code(0x36));
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk) {   // dV += P^T dO ; dK += dS^T Q   (K = queries; 16 = 8 cols)
+          for (int kk = 0; kk < BQ / 16; ++kk)     // K = queries; 16 queries = 8 TMEM columns
             umma_ts(tmem + kColDV, tmem + kColP + kk * 8, do_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(pt_free);
+          // dK += dS^T Q
+          mbar_wait(ds_full, i & 1, abort_flag, p.status, status_code(0x40));
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)
             umma_ts(tmem + kColDK, tmem + kColDS + kk * 8, q_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&q_empty[s]);
+          umma_commit(&q_empty[s]);   // Q and dO of the stage are read
           if (i > 0) {
             mbar_wait(dq_free, (i - 1) & 1, abort_flag, p.status, status_code(0x37));
             tc_fence_after();
@@ -365,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)    // dQ^T = K^T dS^T   (K = keys)
             umma_ss(tmem + kColDQ, dK_mn + kk * 16 * 128, dDS_mn + kk * 16 * 128, id_q, kk > 0);
-          umma_commit(p_free);
+          umma_commit(ds_free);
           umma_commit(dq_full);
         }
         umma_commit(kdv_done);
@@ -464,6 +474,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int j = 0; j < kHalf; ++j) x[j] = ex2(x[j]);     // P^T
+      // P^T (times the dropout multiplier) to TMEM now, so dV(i) runs while dS is computed
+      {
+        uint32_t pp[kHalf / 2];
+#pragma unroll
+        for (int c = 0; c < kHalf / 2; ++c) {
+          if (DROP) {
+            const float m0 = ((col >> (2 * c)) & 1u) ? p.drop.scale : 0.f;
+            const float m1 = ((col >> (2 * c + 1)) & 1u) ? p.drop.scale : 0.f;
+            pp[c] = pack_bf16x2(x[2 * c] * m0, x[2 * c + 1] * m1);
+          } else {
+            pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
+          }
+        }
+        if (i > 0) {   // dV(i-1) has read the previous P^T
+          mbar_wait(pt_free, (i - 1) & 1, abort_flag, p.status, status_code(0x3b));
+          tc_fence_after();
+        }
+        tmem_st16(tmem + lane_off + kColP + hf * (kHalf / 2), pp);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pt_full);
+      }
       float nd[kHalf];   // -D of this warp's 32 queries
 #pragma unroll
       for (int c = 0; c < kHalf / 4; ++c) {
@@ -482,15 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dp_free);
-      uint32_t pp[kHalf / 2], pd[kHalf / 2];
+      uint32_t pd[kHalf / 2];
       if (DROP) {
-        // dropout: dS^T = P^T (dP^T o m - D), dV takes (P o m)^T, m = keep / (1 - p)
+        // dropout: dS^T = P^T (dP^T o m - D) (dV took (P o m)^T above), m = keep / (1 - p)
 #pragma unroll
         for (int j = 0; j < kHalf; ++j) {
           const float mj = ((col >> j) & 1u) ? p.drop.scale : 0.f;
-          const float xm = x[j] * mj;
           d[j] = x[j] * fmaf(d[j], mj, nd[j]);
-          x[j] = xm;
         }
       } else {
 #pragma unroll
@@ -501,15 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll
-      for (int c = 0; c < kHalf / 2; ++c) {
-        pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
-        pd[c] = pack_bf16x2(d[2 * c], d[2 * c + 1]);
-      }
-      if (i > 0) {
-        mbar_wait(p_free, (i - 1) & 1, abort_flag, p.status, status_code(0x3b));
+      for (int c = 0; c < kHalf / 2; ++c) pd[c] = pack_bf16x2(d[2 * c], d[2 * c + 1]);
+      if (i > 0) {   // dK(i-1) and dQ^T(i-1) have read the previous dS^T
+        mbar_wait(ds_free, (i - 1) & 1, abort_flag, p.status, status_code(0x41));
         tc_fence_after();
       }
-      tmem_st16(tmem + lane_off + kColP + hf * (kHalf / 2), pp);
       tmem_st16(tmem + lane_off + kColDS + hf * (kHalf / 2), pd);
 #pragma unroll
       for (int c = 0; c < kHalf / 8; ++c) {
@@ -521,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(ds_full);
     }
     // ---------------------------------------------------------- dK, dV epilogue (one column half writes)
     if (hf == 0) {
