@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 METRIC = "SDPA fwd/bwd TFLOP/s and % of GB300 bf16 peak; decode HBM GB/s"
 MAIN = "gqa_causal_e128"
 DECODE = "gqa_decode_s32k"
+NOMINAL_BF16_TFLOPS = 2250.0   # dense bf16 tensor rate of the part (context beside the measured peak)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 
@@ -347,9 +348,11 @@ def run_ours(args, ws, rank, local):
     phases = {
         "fwd": {"ms": round(t_fwd, 4), "tflops": round(f_fwd / (t_fwd * 1e-3) / 1e12, 2),
                 "frac_of_bf16_peak": round(f_fwd / (t_fwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "frac_of_2250_nominal": round(f_fwd / (t_fwd * 1e-3) / 1e12 / NOMINAL_BF16_TFLOPS, 4),
                 "kernel": "fwd_tc_kernel" if fwd_tc else "fwd_simt_kernel", "launches_per_step": fwd_launches},
         "bwd": {"ms": round(t_bwd, 4), "tflops": round(f_bwd / (t_bwd * 1e-3) / 1e12, 2),
                 "frac_of_bf16_peak": round(f_bwd / (t_bwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "frac_of_2250_nominal": round(f_bwd / (t_bwd * 1e-3) / 1e12 / NOMINAL_BF16_TFLOPS, 4),
                 "kernel": "bwd_tc_kernel" if bwd_tc else "bwd_dq_simt_kernel+bwd_dkdv_simt_kernel",
                 "launches_per_step": bwd_launches},
     }
