@@ -76,7 +76,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "default_scale", "ref_forward", "ref_backward", "ref_forward_rows",
+    "default_scale", "ref_forward", "ref_backward", "ref_forward_rows", "ref_backward_rows",
     "ref_group", "causal_bias", "band_bias", "Band", "gather_paged", "ref_forward_paged",
     "philox4x32_10", "dropout_keep", "Dropout",
 ]
@@ -420,6 +420,37 @@ def ref_forward_rows(q, k, v, b, h, rows, mask=None, scale=None, is_causal=False
     if dropout is not None and dropout.p > 0.0:
         P = P * (dropout_keep(dropout, b * q.shape[1] + h, rows, S) / (1.0 - dropout.p))
     return P @ vh, lse
+
+
+def ref_backward_rows(q, k, v, dO, b, h, rows, mask=None, scale=None, is_causal=False,
+                      enable_gqa=False, band=None):
+    """dQ of selected query rows of one (b, h): for sampled checks of large runs.
+
+    Row i of dQ needs only row i of P, dP = dO V^T and D (course chapter,
+    section 2.3: dS_i = P_i o (dP_i - D_i), D_i = sum_j P_ij dP_ij, dQ_i =
+    alpha dS_i K), so, like the forward's rows, it is a closed sub-problem.
+    """
+    G = q.shape[1] // k.shape[1]
+    kv = h // G
+    rows = np.asarray(rows)
+    L, S, E = q.shape[2], k.shape[2], q.shape[3]
+    alpha = _alpha(scale, E)
+    qh = _as64(q[b, h][rows])
+    kh = _as64(k[b, kv])
+    vh = _as64(v[b, kv])
+    dOh = _as64(dO[b, h][rows])
+    bias = np.zeros((len(rows), S))
+    if mask is not None:
+        m = mask[min(b, mask.shape[0] - 1), min(h, mask.shape[1] - 1)]
+        bias = bias + _as64(m[rows])
+    if is_causal:
+        bias = bias + causal_bias(L, S)[rows]
+    if band is not None:
+        bias = bias + band_bias(L, S, band, b)[rows]
+    P, _ = _masked_softmax(_scores(qh, kh, alpha), bias)
+    dP = dOh @ vh.T
+    dS = _softmax_vjp(P, dP, _row_D(P, dP))
+    return _dq(dS, kh, alpha)
 
 
 def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False, band=None):

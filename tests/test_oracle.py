@@ -439,3 +439,27 @@ def test_group_and_rows_helpers_match_full():
     Or, Lr = oracle.ref_forward_rows(q, k, v, 1, 3, [0, 4, 5], mask, 0.5, True, True)
     np.testing.assert_allclose(Or, O[1, 3, [0, 4, 5]], atol=1e-13)
     np.testing.assert_allclose(Lr, L[1, 3, [0, 4, 5]], atol=1e-13)
+    dQr = oracle.ref_backward_rows(q, k, v, dO, 1, 3, [0, 4, 5], mask, 0.5, True, True)
+    np.testing.assert_allclose(dQr, dQ[1, 3, [0, 4, 5]], atol=1e-13)
+    band = oracle.Band([6, 4], [7, 5], "bottom_right", 0, 3)
+    dQb = oracle.ref_backward(q, k, v, dO, mask, 0.5, False, True, band=band)[0]
+    dQrb = oracle.ref_backward_rows(q, k, v, dO, 0, 1, [1, 2, 5], mask, 0.5, False, True, band=band)
+    np.testing.assert_allclose(dQrb, dQb[0, 1, [1, 2, 5]], atol=1e-13)
+
+
+def test_repeated_keys_equal_log_multiplicity_bias():
+    """Attention over keys that repeat (key r present n_r times, in any order) equals
+    attention over the distinct keys with the additive bias ln n_r: each distinct key's
+    weight is n_r e^(s_r) / sum_r n_r e^(s_r) either way.  Large-size GPU tests rely on it."""
+    rng = np.random.default_rng(81)
+    P, E, Ev = 5, 4, 3
+    counts = np.array([1, 3, 2, 4, 1])
+    kb, vb = rng.standard_normal((P, E)), rng.standard_normal((P, Ev))
+    q = rng.standard_normal((1, 2, 3, E))
+    order = rng.permutation(np.repeat(np.arange(P), counts))
+    k_full, v_full = kb[order][None, None], vb[order][None, None]
+    O1, L1 = oracle.ref_forward(q, k_full, v_full, None, 0.7, False, True)
+    bias = np.broadcast_to(np.log(counts).astype(np.float64), (1, 1, 3, P)).copy()   # [1, 1, L, P]
+    O2, L2 = oracle.ref_forward(q, kb[None, None], vb[None, None], bias, 0.7, False, True)
+    np.testing.assert_allclose(O1, O2, atol=1e-13)
+    np.testing.assert_allclose(L1, L2, atol=1e-13)
