@@ -89,7 +89,13 @@ typedef struct {
  * A bf16 call with L == 1 (E, Ev in {64, 128}) runs the split-KV decode (same
  * contract as sdpa_decode with num_splits = 0) and needs the workspace
  * reported by sdpa_forward_workspace_bytes; every other call needs none
- * (workspace may then be NULL with workspace_bytes = 0). */
+ * (workspace may then be NULL with workspace_bytes = 0).  A bf16 prefill call
+ * on the tensor cores (E, Ev in {64, 128}) with padding lengths
+ * (sdpa_forward_opts) uses the workspace when it is given (at least
+ * sdpa_forward_workspace_bytes, 16-byte aligned): the call zeroes a counter in
+ * it on the stream and the kernel's CTAs take work units from it in turn,
+ * which evens out sequences of unequal length; without it the units follow a
+ * fixed order.  Both give the same results. */
 sdpa_status sdpa_forward(const sdpa_shape* shape,
                          const void* q, const void* k, const void* v,
                          const float* mask_or_null, double scale,
@@ -98,8 +104,9 @@ sdpa_status sdpa_forward(const sdpa_shape* shape,
                          void* workspace, size_t workspace_bytes,
                          void* stream /* cudaStream_t */);
 
-/* Device workspace bytes sdpa_forward needs for `shape` (0 unless the call is
- * routed to the decode path). */
+/* Device workspace bytes sdpa_forward uses for `shape`: the decode path's
+ * partials when it routes there, 256 bytes (a unit counter) for a bf16 prefill
+ * on the tensor cores, 0 otherwise. */
 size_t sdpa_forward_workspace_bytes(const sdpa_shape* shape);
 
 /* Backward of sum(o * dO) (course chapter section 2.3): writes dq [B,Hq,L,E],

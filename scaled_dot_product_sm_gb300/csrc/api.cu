@@ -101,6 +101,9 @@ sdpa_status check_scale(double scale, int E, float* alpha) {
 
 sdpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
 
+// Tensor-core prefill workspace: the unit counter of padded calls (one word, padded).
+constexpr size_t kFwdSchedBytes = 256;
+
 // The band of the plain entry points: no padding, top-left, causal = right bound 0.
 Band plain_band(int is_causal) { return Band{nullptr, nullptr, 0, is_causal ? 0 : -1, 0}; }
 
@@ -350,6 +353,14 @@ sdpa_status forward_impl(const sdpa_shape* shape, const sdpa_options* opts, int 
   p.drop = drop;
   if (c.bf16 && fwd_tc_supported(c.E, c.Ev)) {
     if ((c.L + 255) / 256 > 65535) return SDPA_ERR_UNSUPPORTED;
+    // Padding lengths make the work units uneven: with the workspace the query
+    // reports, the CTAs take units from a counter in it instead of a fixed list.
+    if ((band.seqlen_q || band.seqlen_kv) && workspace && workspace_bytes >= kFwdSchedBytes &&
+        aligned16(workspace)) {
+      p.sched = static_cast<unsigned*>(workspace);
+      const cudaError_t e = cudaMemsetAsync(p.sched, 0, sizeof(unsigned), st);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
     return from_cuda(launch_fwd_tc(p, st));
   }
   if ((c.L + 15) / 16 > 65535 || static_cast<long long>(c.B) * c.Hq > 65535) return SDPA_ERR_UNSUPPORTED;
@@ -484,7 +495,7 @@ sdpa_status sdpa_forward_opts(const sdpa_shape* shape, const sdpa_options* optio
 size_t sdpa_forward_workspace_bytes(const sdpa_shape* shape) {
   Checked c;
   if (check_shape(shape, 1, false, &c) != SDPA_OK) return 0;
-  if (!routes_to_decode(c)) return 0;
+  if (!routes_to_decode(c)) return c.bf16 && fwd_tc_supported(c.E, c.Ev) ? kFwdSchedBytes : 0;
   int nsplit, kps;
   split_layout(c, auto_splits(c), &nsplit, &kps);
   return decode_ws(c, nsplit);

@@ -133,6 +133,9 @@ struct FwdParams {
   Band band;             // padding and diagonal band (top-left causal = right bound 0)
   DropoutParams drop;
   unsigned* status;
+  // tensor-core prefill: nullptr = every CTA walks a fixed list of work units; else a
+  // zeroed device counter from which the CTAs take units in turn (uneven work: padding)
+  unsigned* sched = nullptr;
 };
 
 struct BwdParams {

@@ -79,7 +79,7 @@ struct FwdCfg {
   static constexpr int kOffRing = kOffQ + 2 * kQBytes;
   static constexpr int kOffMask = kOffRing + NS * kItem;
   static constexpr int kOffBar = kOffMask + kMaskBytes;
-  static constexpr int kBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
+  static constexpr int kBytes = kOffBar + 512 + 1024;   // barriers, unit slots + alignment slack
   static_assert(NS >= 2, "the K/V ring needs two stages");
 };
 
@@ -102,7 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_final = p_full + 2;        // 2: the last PV_t of the unit complete
   uint64_t* mk_full = o_final + 2;       // 2: staged mask tile of query tile t landed
   uint64_t* mk_empty = mk_full + 2;      // 2: ... and read by tile t's softmax warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mk_empty + 2);
+  uint64_t* un_full = mk_empty + 2;      // 4: unit index published (taken from the counter)
+  uint64_t* un_empty = un_full + 4;      // 4: ... and read by every role
+  int* un_slot = reinterpret_cast<int*>(un_empty + 4);                  // 4 unit indices
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(un_slot + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,6 +120,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = gridDim.x, c = blockIdx.x;
     const int k = r * G + ((r & 1) ? G - 1 - c : c);
     return k < total ? k : -1;
+  };
+  // With a counter (p.sched), the CTAs take units in turn instead: the producer
+  // thread takes each index and publishes it through a 4-slot ring, and the MMA
+  // thread, the softmax warps and the mask producer read the same sequence.  A
+  // wait that gives up (abort) reads whatever the slot holds: a stale unit index
+  // or the initial -1, never an out-of-range one.
+  const bool dyn = p.sched != nullptr;
+  auto take_unit = [&](int r) {   // producer thread
+    if (!dyn) return unit_index(r);
+    const int sl = r & 3;
+    mbar_wait(&un_empty[sl], ((r >> 2) & 1) ^ 1, abort_flag, p.status, status_code(0x1d));
+    const unsigned tk = atomicAdd(p.sched, 1u);
+    const int k = tk < static_cast<unsigned>(total) ? static_cast<int>(tk) : -1;
+    un_slot[sl] = k;
+    mbar_arrive(&un_full[sl]);   // release: the slot's value is visible to the waiters
+    return k;
+  };
+  auto read_unit = [&](int r) {   // other roles; the caller then reports the read on un_empty
+    if (!dyn) return unit_index(r);
+    const int sl = r & 3;
+    mbar_wait(&un_full[sl], (r >> 2) & 1, abort_flag, p.status, status_code(0x1e));
+    return *reinterpret_cast<volatile int*>(&un_slot[sl]);
   };
   // Key tiles of a unit: tile t (rows rt..rt+127) needs key tiles [a_t, b_t),
   // from lo(rt) to hi(last row before Lb) (padding and band; empty when no row
@@ -168,6 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&mk_full[t], 1);
       mbar_init(&mk_empty[t], 4);
     }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&un_full[i], 1);
+      mbar_init(&un_empty[i], 9 + (MK == kMaskStaged ? 1 : 0));   // MMA thread, 8 softmax warps, mask producer
+      un_slot[i] = -1;
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -188,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmV);
       int it = 0;   // ring position, continued across units
       for (int r = 0;; ++r) {
-        const int k = unit_index(r);
+        const int k = take_unit(r);
         if (k < 0) break;
         const Unit u = unit_at(k);
         // the previous unit's S MMAs have read its Q tiles
@@ -244,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;               // ring position, continued across units
       uint32_t pc[2] = {0, 0};  // p_full completions consumed per tile
       for (int r = 0;; ++r) {
-        const int k = unit_index(r);
+        const int k = read_unit(r);
+        if (dyn) mbar_arrive(&un_empty[r & 3]);
         if (k < 0) break;
         const Unit u = unit_at(k);
         mbar_wait(bar_q, r & 1, abort_flag, p.status, status_code(0x12));
@@ -312,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long LS = static_cast<long long>(p.L) * p.S;
       int cnt[2] = {0, 0}, last = -1;
       for (int ur = 0;; ++ur) {
-        const int k = unit_index(ur);
+        const int k = read_unit(ur);
+        if (dyn) mbar_arrive(&un_empty[ur & 3]);
         if (k < 0) break;
         const Unit u = unit_at(k);
         const int slice = static_cast<int>((u.b * p.mask_sb + u.h * p.mask_sh) / LS);
@@ -349,7 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sc_cnt = 0, oc_cnt = 0;       // s_full / o_final completions consumed
     uint32_t mk_cnt = 0;                   // staged mask tiles of this query tile consumed
     for (int ur = 0;; ++ur) {
-      const int k = unit_index(ur);
+      const int k = read_unit(ur);
+      if (dyn) {   // every lane has read the slot before it is reported free
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&un_empty[ur & 3]);
+      }
       if (k < 0) break;
       const Unit u = unit_at(k);
       const int row_first = u.r0 + t * BM;   // first row of this tile

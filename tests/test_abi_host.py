@@ -120,8 +120,10 @@ def test_decode_workspace_and_splits(lib):
         assert ws >= rows * splits * (128 + 1) * 4
     assert lib.sdpa_forward_workspace_bytes(ctypes.byref(shp)) == lib.sdpa_decode_workspace_bytes(
         ctypes.byref(shp), 0)
-    # prefill needs no forward workspace
-    assert lib.sdpa_forward_workspace_bytes(ctypes.byref(_shape(L=64))) == 0
+    # bf16 prefill on the tensor cores: a unit counter (used by padded calls); fp32 and other widths: none
+    assert lib.sdpa_forward_workspace_bytes(ctypes.byref(_shape(L=64))) == 256
+    assert lib.sdpa_forward_workspace_bytes(ctypes.byref(_shape(L=64, dtype=0))) == 0
+    assert lib.sdpa_forward_workspace_bytes(ctypes.byref(_shape(L=64, E=32, Ev=32))) == 0
     # decode rejects a negative split count and a too-small workspace before launching
     st = lib.sdpa_decode(ctypes.byref(shp), P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 1, -1, P(FAKE),
                          P(FAKE), P(FAKE), 1 << 30, None)

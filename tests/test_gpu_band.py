@@ -139,3 +139,22 @@ def test_plain_causal_equals_top_left_right_bound_zero():
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
     d = (g1[0].float() - g2[0].float()).norm() / g1[0].float().norm()
     assert d <= 1e-3, d
+
+
+def test_padded_counter_schedule_equals_fixed_order():
+    """With padding lengths the tensor-core forward takes work units from a counter in its
+    workspace; without a workspace it walks a fixed list.  Units are independent, so both
+    give bit-identical outputs, and both match the oracle."""
+    B, Hq, Hkv, L, S, E = 6, 8, 2, 1100, 1100, 128
+    lq, lk = [1100, 37, 900, 0, 640, 1], [1100, 500, 900, 10, 1100, 1]
+    q, k, v, _, _ = random_inputs(B, Hq, Hkv, L, S, E, E, torch.bfloat16, seed=230)
+    ob, gb = _bands(B, lq, lk, "bottom_right", 0, None)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = sdpa.sdpa_forward(qd, kd, vd, None, None, False, True, band=gb)   # counter (workspace given)
+    none = torch.empty(0, dtype=torch.uint8, device="cuda")
+    o2, l2 = sdpa.sdpa_forward(qd, kd, vd, None, None, False, True, band=gb, workspace=none)
+    torch.cuda.synchronize()
+    assert sdpa.last_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ref_o, ref_lse = oracle.ref_forward(q, k, v, None, None, False, True, band=ob)
+    check_forward(o1, lse=l1, ref_o=ref_o, ref_lse=ref_lse, bf16=True)
