@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb = j * BN;
         float x[BN];
         if (MASKED) {   // the TMEM loads below are executed by the whole warp in either branch
-          // mask * log2e for this row's keys, read before the scores land so the
+          // the mask values of this row's keys, read before the scores land so the
           // loads' latency overlaps the wait; whole 32-byte sectors when the rows
           // are 32-byte aligned (S a multiple of 8), else 16-byte or scalar loads.
           // Rows past L (mrow == nullptr) read nothing.  Staged: the row from shared
@@ -431,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
                 const float4 mv = *reinterpret_cast<const float4*>(ms + q * (BM * 128) + ((c ^ (r & 7)) << 4));
-                x[32 * q + 4 * c + 0] = mv.x * kLog2e;
-                x[32 * q + 4 * c + 1] = mv.y * kLog2e;
-                x[32 * q + 4 * c + 2] = mv.z * kLog2e;
-                x[32 * q + 4 * c + 3] = mv.w * kLog2e;
+                x[32 * q + 4 * c + 0] = mv.x;
+                x[32 * q + 4 * c + 1] = mv.y;
+                x[32 * q + 4 * c + 2] = mv.z;
+                x[32 * q + 4 * c + 3] = mv.w;
               }
             // the next fill is a TMA (async-proxy) write: order this lane's reads before it
             fence_proxy_async_smem();
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u8 = 0; u8 < 8; ++u8) m8[u8] = 0.f;
               }
 #pragma unroll
-              for (int u8 = 0; u8 < 8; ++u8) x[8 * c + u8] = m8[u8] * kLog2e;
+              for (int u8 = 0; u8 < 8; ++u8) x[8 * c + u8] = m8[u8];
             }
           } else if ((p.S & 3) == 0) {
 #pragma unroll
@@ -464,14 +464,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int key = kb + 4 * c;
               const float4 mv = mrow && key < p.S ? __ldg(reinterpret_cast<const float4*>(mrow + key))
                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-              x[4 * c + 0] = mv.x * kLog2e;
-              x[4 * c + 1] = mv.y * kLog2e;
-              x[4 * c + 2] = mv.z * kLog2e;
-              x[4 * c + 3] = mv.w * kLog2e;
+              x[4 * c + 0] = mv.x;
+              x[4 * c + 1] = mv.y;
+              x[4 * c + 2] = mv.z;
+              x[4 * c + 3] = mv.w;
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < BN; ++i) x[i] = mrow && kb + i < p.S ? __ldg(mrow + kb + i) * kLog2e : 0.f;
+            for (int i = 0; i < BN; ++i) x[i] = mrow && kb + i < p.S ? __ldg(mrow + kb + i) : 0.f;
           }
           mbar_wait(&s_full[t], sc_cnt & 1, abort_flag, p.status, status_code(0x18));
           ++sc_cnt;
@@ -481,9 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t v[32];
             tmem_ld32(tS + c * 32, v);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              fma2(x[c * 32 + i], x[c * 32 + i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sc, sc,
-                   x[c * 32 + i], x[c * 32 + i + 1]);
+            for (int i = 0; i < 32; i += 2)   // t = s * alpha + mask (natural-log units)
+              fma2(x[c * 32 + i], x[c * 32 + i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), p.scale,
+                   p.scale, x[c * 32 + i], x[c * 32 + i + 1]);
           }
         } else {
           mbar_wait(&s_full[t], sc_cnt & 1, abort_flag, p.status, status_code(0x18));
@@ -512,7 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u8 = 0; u8 < 8; ++u8) mx8[u8] = max3f(mx8[u8], x[i + u8], x[i + 8 + u8]);
         const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
                                fmaxf(mx8[6], mx8[7]));
-        const float m_new = fmaxf(m_run, MASKED ? mx : mx * sc);
+        // to log2 units: raw scores times alpha*log2(e), or the masked t times log2(e)
+        const float xs = MASKED ? kLog2e : sc;
+        const float m_new = fmaxf(m_run, mx * xs);
         const bool need = m_new > m_run + kRescaleThreshold;
         const float m_use = need ? m_new : m_run;
         const float nm = (m_use == kNegInf) ? 0.f : -m_use;
@@ -523,10 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < BN; i += 2) {
           float a0, a1;
-          if (MASKED)
-            add2(a0, a1, x[i], x[i + 1], nm, nm);        // x already scaled (and the mask added)
-          else
-            fma2(a0, a1, x[i], x[i + 1], sc, sc, nm, nm);  // s*sc - m
+          fma2(a0, a1, x[i], x[i + 1], xs, xs, nm, nm);   // x * xs - m
           a0 = ex2(a0);
           a1 = ex2(a1);
           const int q4 = (i >> 1) & 3;
