@@ -300,6 +300,14 @@ sdpa_status sdpa_decode_paged(const sdpa_shape* shape, const sdpa_options* optio
 /* Static, NUL-terminated description of a status code. */
 const char* sdpa_status_string(sdpa_status status);
 
+/* Failure-path self-test: launches, on `stream`, one CTA whose thread waits on an
+ * mbarrier that nothing ever arrives at.  The wait is bounded like every wait in
+ * the kernels: it gives up after its limit (about a second), records
+ * SDPA_ERR_TIMEOUT in the device status word and the kernel returns normally, so
+ * the context stays usable.  Returns the launch's status; the caller then reads
+ * sdpa_last_device_status() (SDPA_ERR_TIMEOUT once, then SDPA_OK). */
+sdpa_status sdpa_selftest_wait_timeout(void* stream /* cudaStream_t */);
+
 /* Reads and clears the current device's status word that kernels set when a
  * bounded device-side wait gives up.  Returns SDPA_OK when no kernel has timed
  * out since the last call.  Synchronises the device first (call it off the

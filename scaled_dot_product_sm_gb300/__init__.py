@@ -20,7 +20,7 @@ __all__ = [
     "SdpaError", "load_library", "exported_symbols", "sdpa_forward", "sdpa_backward", "sdpa_decode",
     "forward_workspace_bytes", "backward_workspace_bytes", "decode_workspace_bytes",
     "decode_num_splits", "last_device_status", "Shape", "Options", "Band", "Dropout", "PagedKV",
-    "sdpa_decode_paged",
+    "sdpa_decode_paged", "selftest_wait_timeout",
     "build", "LIB_PATH",
 ]
 
@@ -32,7 +32,7 @@ EXPORTS = (
     "sdpa_forward", "sdpa_forward_workspace_bytes", "sdpa_backward", "sdpa_backward_workspace_bytes",
     "sdpa_decode", "sdpa_decode_workspace_bytes", "sdpa_decode_num_splits", "sdpa_status_string",
     "sdpa_last_device_status", "sdpa_decode_noalloc", "sdpa_forward_opts", "sdpa_backward_opts",
-    "sdpa_decode_opts", "sdpa_decode_paged",
+    "sdpa_decode_opts", "sdpa_decode_paged", "sdpa_selftest_wait_timeout",
 )
 
 
@@ -149,6 +149,8 @@ def load_library(path: Optional[str] = None):
     lib.sdpa_status_string.restype = ctypes.c_char_p
     lib.sdpa_last_device_status.argtypes = []
     lib.sdpa_last_device_status.restype = ctypes.c_int
+    lib.sdpa_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
+    lib.sdpa_selftest_wait_timeout.restype = ctypes.c_int
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -375,6 +377,15 @@ def sdpa_decode_paged(q, k_container, v_container, page_table_k, page_table_v, S
 def last_device_status() -> int:
     """Reads and clears the device status word (synchronises the device)."""
     return int(load_library().sdpa_last_device_status())
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Runs the failure-path self-test kernel (a bounded wait that nothing satisfies: it gives
+    up after about a second and records a timeout); read last_device_status() afterwards."""
+    import torch
+    lib = load_library()
+    st = ctypes.c_void_p(stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+    _raise(lib.sdpa_selftest_wait_timeout(st), "sdpa_selftest_wait_timeout")
 
 
 def default_scale(E: int) -> float:

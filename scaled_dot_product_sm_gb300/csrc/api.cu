@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "sdpa.h"
 
 namespace sdpa_impl {
@@ -100,6 +101,21 @@ sdpa_status check_scale(double scale, int E, float* alpha) {
 }
 
 sdpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
+
+// Failure-path self-test: one thread waits on an mbarrier nothing arrives at; the
+// bounded wait gives up after its limit, records a timeout in the status word and
+// the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(unsigned* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    sdpa_ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    sdpa_ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sdpa_ptx::mbar_wait(&bar, 0, &abort_flag, status, status_code(0x7f));
+}
 
 // Tensor-core prefill workspace: the unit counter of padded calls (one word, padded).
 constexpr size_t kFwdSchedBytes = 256;
@@ -581,6 +597,13 @@ const char* sdpa_status_string(sdpa_status status) {
     case SDPA_ERR_TIMEOUT: return "device-side wait timed out";
   }
   return "unknown status";
+}
+
+sdpa_status sdpa_selftest_wait_timeout(void* stream) {
+  unsigned* status = status_ptr();
+  if (!status) return SDPA_ERR_CUDA;
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+  return from_cuda(cudaGetLastError());
 }
 
 sdpa_status sdpa_last_device_status(void) {

@@ -308,6 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                       b * a.mslice_b + (hkv * p.G + g) * a.mslice_h);
         }
       }
+      if (*abort_flag) {   // a wait gave up: let this thread's copies land before the CTA exits
+        mbar_drain(kv_full, 0);
+        mbar_drain_ring(q_full, kNSQ, n);
+        if (MSTAGE) mbar_drain(m_full, static_cast<uint32_t>((n - 1) & 1));
+      }
     } else if ((warp == 13 || warp == 14) && lane == 0 && n > 0) {
       // ---------------------------------------------------------- MMA issuers
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T: K-major x K-major

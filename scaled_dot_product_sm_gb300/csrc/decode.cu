@@ -183,6 +183,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         }
       }
     }
+    // a wait gave up: let this warp's copies land before the CTA exits
+    if (lane == 0 && *abort_flag) mbar_drain_ring(full, NSTAGE, nst);
   } else {
     // ------------------------------------------------------------ consumers
     // Q^T as the MMA's B operand (k = E, n = row): lane holds row n = lane/4,

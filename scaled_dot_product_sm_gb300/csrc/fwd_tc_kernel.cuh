@@ -216,11 +216,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      int it = 0;   // ring position, continued across units
+      int it = 0;       // ring position, continued across units
+      int nunits = 0;   // units whose Q tiles were requested (one bar_q phase each)
       for (int r = 0;; ++r) {
         const int k = take_unit(r);
         if (k < 0) break;
         const Unit u = unit_at(k);
+        ++nunits;
         // the previous unit's S MMAs have read its Q tiles
         mbar_wait(q_free, (r & 1) ^ 1, abort_flag, p.status, status_code(0x10));
         const int nq = (u.e[0] > u.a[0]) + (u.e[1] > u.a[1]);
@@ -247,6 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           load(false, j);
           if (j + 1 < u.j1) load(true, j + 1);
         }
+      }
+      if (*abort_flag) {   // a wait gave up: let this thread's copies land before the CTA exits
+        if (nunits > 0) mbar_drain(bar_q, static_cast<uint32_t>((nunits - 1) & 1));
+        mbar_drain_ring(full, NS, it);
       }
     } else if (warp == 9 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -364,6 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (*abort_flag)   // a wait gave up: let this thread's copies land before the CTA exits
+        for (int t = 0; t < 2; ++t)
+          if (cnt[t] > 0) mbar_drain(&mk_full[t], static_cast<uint32_t>((cnt[t] - 1) & 1));
     }
   } else {
     regs_inc<kRegsSoftmax>();

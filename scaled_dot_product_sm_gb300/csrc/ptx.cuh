@@ -74,6 +74,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// After a wait gave up (the CTA's abort flag is set), a thread that issued TMA
+// copies waits, with a bound of its own and whatever the flag says, until the
+// last phase of each barrier those copies signal has completed, so that no copy
+// still writes into shared memory when the CTA exits.  The bound (about 0.1 s)
+// keeps even a copy that never lands from holding the CTA.
+constexpr long long kDrainLimitCycles = 200000000LL;
+
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity))
+    if (clock64() - t0 > kDrainLimitCycles) return;
+}
+
+// The same for a ring of `ns` barriers that received `issued` fills in turn
+// (fill i went to barrier i % ns, as phase i / ns).
+__device__ __forceinline__ void mbar_drain_ring(uint64_t* full, int ns, long long issued) {
+  for (int s = 0; s < ns && s < issued; ++s) {
+    const long long last = s + ns * ((issued - 1 - s) / ns);
+    mbar_drain(&full[s], static_cast<uint32_t>((last / ns) & 1));
+  }
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
