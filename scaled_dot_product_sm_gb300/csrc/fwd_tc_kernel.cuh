@@ -7,14 +7,16 @@
 //
 // A work unit = one (batch, query head) and two 128-row query tiles (256 rows)
 // that share every K/V tile load.  The grid is persistent (one CTA per SM, each
-// walking a list of units), so the next unit's Q load and first scores overlap
-// the current unit's last tiles and epilogue.  Warp roles (384 threads, three
+// walking a list of units, or taking them from a counter when padding lengths
+// make them uneven), so the next unit's Q load and first scores overlap the
+// current unit's last tiles and epilogue.  Warp roles (384 threads, three
 // warpgroups):
 //   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax of query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through a ring
 //   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp  10   stages the additive mask by TMA (rows of a multiple of 4 keys), else idle
+//   warp  11   idle (it completes the third warpgroup)
 // The third warpgroup hands registers to the softmax warpgroups (72 -> 216 per
 // thread: 4*32*72 + 8*32*216 = 64512 = 384*168, the launch's register file share).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+Ev), O_1 [384,384+Ev).
@@ -26,7 +28,7 @@
 // S_t(j+1) (which overwrites P_t(j)'s columns) follows PV_t(j) in the same
 // in-order MMA stream.  The commit after S_t(j+1) also covers PV_t(j), so when
 // tile t sees its next scores, O_t is complete.  Exponentials are exp2 with alpha*log2(e)
-// folded into the scale; O is only rescaled when a row's max grows by more
+// folded into the scale (with a mask, log2(e) into the exponent's FMA); O is only rescaled when a row's max grows by more
 // than 2^8 (the stale max keeps every p below 256, and O/l is exact either way).
 // Causal: key tiles entirely above the diagonal are neither loaded nor
 // computed; only tiles that cross it test j <= i per element.
