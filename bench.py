@@ -100,6 +100,12 @@ def barrier(ws):
         dist.barrier()
 
 
+def job_rate(ws, work_per_rank, t_max_ms, unit):
+    """Whole-job rate: every rank did `work_per_rank` (flops or bytes) in parallel, the job
+    took the slowest rank's time (ms); in `unit` (1e12 for TFLOP/s, 1e9 for GB/s)."""
+    return ws * work_per_rank / (t_max_ms * 1e-3) / unit
+
+
 def reduce_max(x, ws):
     if ws == 1:
         return x
@@ -302,7 +308,7 @@ def run_ours(args, ws, rank, local):
     else:
         pairs = visible_pairs(w, spec)
         f_fwd, f_bwd = 4.0 * w.E * pairs, 10.0 * w.E * pairs
-    value = ws * (f_fwd + f_bwd) / (t_step_max * 1e-3) / 1e12
+    value = job_rate(ws, f_fwd + f_bwd, t_step_max, 1e12)
     assert sdpa.last_device_status() == 0
 
     # ---------------------------------------------------------- end to end (host buffers)
@@ -338,7 +344,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         barrier(ws)
         t_e2e = reduce_max(e0.elapsed_time(e1) / args.steps, ws)
-        e2e = {"value": round(ws * (f_fwd + f_bwd) / (t_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e = {"value": round(job_rate(ws, f_fwd + f_bwd, t_e2e, 1e12), 2), "unit": "TFLOP/s",
                "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # ---------------------------------------------------------- launches and roofline
@@ -423,7 +429,7 @@ def run_ours(args, ws, rank, local):
         t_dec = reduce_max(sum(a.elapsed_time(b) for a, b in dev_evs) / args.steps, ws)
         kv_bytes = (kd.numel() + vd.numel()) * kd.element_size()
         io_bytes = kv_bytes + qd.numel() * 2 + od.numel() * 2 + lsed.numel() * 4
-        gbps = ws * io_bytes / (t_dec * 1e-3) / 1e9
+        gbps = job_rate(ws, io_bytes, t_dec, 1e9)
         decode = {"workload": DECODE, "ms": round(t_dec, 4), "gbps": round(gbps, 1),
                   "frac_of_measured_hbm": round(gbps / ws / peaks["hbm_gbs"], 4),
                   "frac_of_8tbs_nominal": round(gbps / ws / 8000.0, 4),
@@ -466,7 +472,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         barrier(ws)
         t_pg = reduce_max(sum(a.elapsed_time(b) for a, b in dev_evs) / args.steps, ws)
-        gbps_pg = ws * io_bytes / (t_pg * 1e-3) / 1e9
+        gbps_pg = job_rate(ws, io_bytes, t_pg, 1e9)
         decode["paged"] = {"block_size": bsz, "layout": "64-key blocks of every sequence shuffled in one container",
                            "ms": round(t_pg, 4), "gbps": round(gbps_pg, 1),
                            "frac_of_measured_hbm": round(gbps_pg / ws / peaks["hbm_gbs"], 4)}
