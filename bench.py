@@ -13,7 +13,9 @@ launching stream, with a 256 MiB L2 flush between steps outside the events;
 a barrier and a device synchronize on both sides of the timed loop; the max
 over ranks.  nvidia-smi clocks are sampled during the timed loop.  "e2e" is
 the same step through the same calls with host (pinned) buffers: inputs copied
-host->device and every output copied device->host inside the timed region.
+host->device and every output copied device->host inside the timed region, on
+copy streams that overlap the copies with the kernels within each step (dO
+comes in during the forward, O and LSE go out during the backward).
 
 --impl reference times the float64 CPU oracle (the parity reference, not a
 tuned CPU implementation) on a bounded sample of the same workload.
@@ -323,13 +325,71 @@ def run_ours(args, ws, rank, local):
         dev_in = (q, k, v, dO) + ((mask,) if mask is not None else ()) + tuple(
             t for t in ((band.seq_len_q, band.seq_len_kv) if band is not None else ()) if t is not None)
 
+        # A step as a user of the stream-taking API runs it: the inputs come in on a copy
+        # stream and the results go out on another, overlapped with the kernels, and the
+        # step ends when the gradients are on the host.  With no dropout or band (whose
+        # counters and lengths are per batch) the batch is pipelined per sequence: batch
+        # b + 1's inputs land while batch b computes.  No copy crosses a step boundary:
+        # the next step's inputs wait for this step's last kernel.
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        per_batch = w.B > 1 and drop is None and band is None
+        nb = w.B if per_batch else 1
+        bsl = [slice(i, i + 1) for i in range(w.B)] if per_batch else [slice(0, w.B)]
+        mb = (lambda t, sl: t[sl]) if (m_h is not None and m_h.shape[0] == w.B) else (lambda t, sl: t)
+        bws_c = [bws] if nb == 1 else [torch.empty(max(16, sdpa.backward_workspace_bytes(q[sl], k[sl], v[sl])),
+                                                   dtype=torch.uint8, device=dev) for sl in bsl]
+        # copied once per step before the batches: the padding lengths, and the mask unless it
+        # is sliced per batch below (one broadcast mask serves every batch)
+        mask_per_batch = mask is not None and per_batch and m_h.shape[0] == w.B
+        extra_in = [(src, dst) for src, dst in list(zip(host, dev_in))[4:] if not (mask_per_batch and dst is mask)]
+
+        def fwd_c(c):
+            sl = bsl[c]
+            sdpa.sdpa_forward(q[sl], k[sl], v[sl], None if mask is None else mb(mask, sl), scale, w.is_causal,
+                              w.enable_gqa, out=o[sl], lse=lse[sl], band=band, dropout=drop)
+
+        def bwd_c(c):
+            sl = bsl[c]
+            sdpa.sdpa_backward(q[sl], k[sl], v[sl], o[sl], dO[sl], lse[sl], None if mask is None else mb(mask, sl),
+                               scale, w.is_causal, w.enable_gqa, dq=dq[sl], dk=dk[sl], dv=dv[sl],
+                               workspace=bws_c[c], band=band, dropout=drop)
+
         def e2e_step():
-            for src, dst in zip(host, dev_in):
-                dst.copy_(src, non_blocking=True)
-            fwd()
-            bwd()
-            for src, dst in zip((o, lse, dq, dk, dv), out_h):
-                dst.copy_(src, non_blocking=True)
+            s_in.wait_stream(stream)
+            ev_f, ev_b = [], []
+            with torch.cuda.stream(s_in):
+                for src, dst in extra_in:
+                    dst.copy_(src, non_blocking=True)
+                for c, sl in enumerate(bsl):
+                    for src, dst in zip(host[:3], (q, k, v)):
+                        dst[sl].copy_(src[sl], non_blocking=True)
+                    if mask_per_batch:
+                        mask[sl].copy_(host[4][sl], non_blocking=True)
+                    ev_f.append(torch.cuda.Event())
+                    ev_f[-1].record(s_in)
+                for c, sl in enumerate(bsl):
+                    dO[sl].copy_(host[3][sl], non_blocking=True)
+                    ev_b.append(torch.cuda.Event())
+                    ev_b[-1].record(s_in)
+            for c, sl in enumerate(bsl):
+                stream.wait_event(ev_f[c])
+                fwd_c(c)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                s_out.wait_event(ev)
+                with torch.cuda.stream(s_out):
+                    out_h[0][sl].copy_(o[sl], non_blocking=True)
+                    out_h[1][sl].copy_(lse[sl], non_blocking=True)
+            for c, sl in enumerate(bsl):
+                stream.wait_event(ev_b[c])
+                bwd_c(c)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                s_out.wait_event(ev)
+                with torch.cuda.stream(s_out):
+                    for src, dst in zip((dq, dk, dv), out_h[2:]):
+                        dst[sl].copy_(src[sl], non_blocking=True)
+            stream.wait_stream(s_out)
 
         for _ in range(args.warmup):
             e2e_step()
