@@ -85,6 +85,9 @@ PREFILL = [
     (1, 2, 2, 400, 400, 128, 128, "bf16", None, None, "top_left", 50, 64, "none"),
     (2, 2, 2, 300, 900, 64, 64, "bf16", [300, 200], [900, 450], "bottom_right", 0, 256, "none"),
     (1, 3, 3, 260, 260, 64, 128, "bf16", None, [200], "top_left", 0, 70, "none"),
+    # rows of a multiple of 4 keys: the additive mask is staged by TMA, the padded units come from the counter
+    (2, 4, 2, 300, 512, 128, 128, "bf16", [300, 200], [512, 256], "bottom_right", 0, 100, "bias"),
+    (3, 2, 2, 260, 388, 64, 64, "bf16", [260, 0, 129], [388, 100, 200], "top_left", 0, None, "bias"),
     (1, 2, 1, 150, 170, 32, 40, "bf16", [150], [120], "bottom_right", 0, 50, "bias"),   # CUDA-core bf16
     (2, 2, 2, 70, 90, 24, 16, "f32", [70, 33], [90, 10], "bottom_right", 0, 20, "bias"),
     (2, 2, 1, 64, 64, 16, 16, "f32", [64, 0], [64, 64], "top_left", 3, 8, "none"),
