@@ -8,7 +8,6 @@ length.  A planted off-by-one in the offset is caught.
 """
 import numpy as np
 import pytest
-import torch
 
 import oracle
 from oracle import sdpa_oracle as so
