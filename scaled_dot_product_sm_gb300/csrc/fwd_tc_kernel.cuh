@@ -367,6 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < BN / 32; ++q)
               tma_load_3d(smem + C::kOffMask + q * (BM * 128), &tmM, &mk_full[t], j * BN + 32 * q, row_first, slice);
+            if (j + 1 < u.e[t])   // the tile's next key tile into L2 now, so its fill is an L2 hit
+#pragma unroll
+              for (int q = 0; q < BN / 32; ++q) tma_prefetch_l2_3d(&tmM, (j + 1) * BN + 32 * q, row_first, slice);
             ++cnt[t];
             last = t;
           }
