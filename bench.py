@@ -404,7 +404,8 @@ def run_ours(args, ws, rank, local):
         barrier(ws)
         t_e2e = reduce_max(e0.elapsed_time(e1) / args.steps, ws)
         e2e = {"value": round(job_rate(ws, f_fwd + f_bwd, t_e2e, 1e12), 2), "unit": "TFLOP/s",
-               "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "gpu_launches_per_step": nb * 4, "batches_pipelined": nb}
 
     # ---------------------------------------------------------- launches and roofline
     bwd_launches = 3   # tensor cores: row stats, main, dQ convert; CUDA cores: pre-pass, dQ, dK/dV
