@@ -188,10 +188,13 @@ def test_bf16_large_scores_no_overflow():
 
 
 # ----------------------------------------------------------------------------- decode
-@pytest.mark.parametrize("splits", [1, 2, 7, 0])
-def test_decode_split_invariance(splits):
-    """Split-KV decode equals the oracle for any split count (merge exact up to fp32 rounding)."""
-    B, Hq, Hkv, S, E = 2, 8, 2, 1000, 128
+@pytest.mark.parametrize("splits,S", [(1, 1000), (2, 1000), (7, 1000), (0, 1000), (64, 4095)])
+def test_decode_split_invariance(splits, S):
+    """Split-KV decode equals the oracle for any split count (merge exact up to fp32 rounding).
+
+    With 64-key stages, S = 4095 and 64 requested splits give 64 splits of 64 keys,
+    the last one 63."""
+    B, Hq, Hkv, E = 2, 8, 2, 128
     q, k, v, _, _ = random_inputs(B, Hq, Hkv, 1, S, E, E, torch.bfloat16, seed=11)
     ref_o, ref_lse = oracle.ref_forward(q, k, v, None, None, False, True)
     o, lse = sdpa.sdpa_decode(q.cuda(), k.cuda(), v.cuda(), None, None, True, splits)
