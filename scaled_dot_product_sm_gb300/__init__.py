@@ -3,12 +3,19 @@
 Argument marshalling only: shapes and device pointers of torch tensors are
 passed to the C ABI declared in include/sdpa.h, outputs and workspaces are
 allocated with torch on the inputs' device, and work is enqueued on torch's
-current CUDA stream.  Every step of the computation runs in the library's
-CUDA kernels; there is no fallback.  Importing works without a GPU; calling
-needs the built library (``build()``) and a CUDA device, and raises otherwise.
+current CUDA stream of that device.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback.  Importing works without a GPU;
+calling needs the built library (``build()``) and a CUDA device, and raises
+otherwise.
+
+The C ABI receives plain pointers and one shape, so it cannot see a tensor whose
+extents disagree with that shape.  The binding therefore checks every tensor's
+shape, dtype, device and contiguity against the shape derived from q, k and v
+(ValueError) before it loads the library or launches anything.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -69,9 +76,12 @@ class Band:
         self.seq_len_q, self.seq_len_kv = seq_len_q, seq_len_kv
         self.alignment, self.right_bound, self.left_bound = alignment, right_bound, left_bound
 
-    def options(self, dropout=None) -> Options:
+    def options(self, dropout=None, batch: Optional[int] = None) -> Options:
+        """The sdpa_options struct; batch, when given, is the call's B, which each length tensor must match."""
         import torch
         for t in (self.seq_len_q, self.seq_len_kv):
+            if t is not None and batch is not None and (t.dim() != 1 or t.numel() != batch):
+                raise ValueError(f"seq_len tensors must hold B = {batch} lengths, got shape {tuple(t.shape)}")
             if t is not None and (not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous()):
                 raise ValueError("seq_len tensors must be contiguous CUDA int32")
         align = {"top_left": 0, "bottom_right": 1}.get(self.alignment)
@@ -178,21 +188,49 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
 
 
-def _shape(q, k, v, mask) -> Shape:
+def _expect(t, name, shape, dtype):
+    """Raises ValueError unless t (if given) has exactly this shape and dtype."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(int(x) for x in shape)}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check_mask(mask, L, S):
+    """The additive mask is fp32 [mask_b, mask_h, L, S]; the library checks mask_b and mask_h."""
+    import torch
+    if mask is None:
+        return
+    if mask.dim() != 4:
+        raise ValueError("mask must be 4-D [B|1, Hq|1, L, S]")
+    _expect(mask, "mask", (mask.shape[0], mask.shape[1], L, S), torch.float32)
+
+
+def _check_qkv(q, k, v, mask):
+    """q [B,Hq,L,E], k [B,Hkv,S,E], v [B,Hkv,S,Ev] of one dtype, and the mask."""
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, H, T, D]")
     B, Hq, L, E = q.shape
     _, Hkv, S, _ = k.shape
+    _expect(k, "k", (B, Hkv, S, E), q.dtype)
+    _expect(v, "v", (B, Hkv, S, v.shape[3]), q.dtype)
+    _check_mask(mask, L, S)
+
+
+def _shape(q, k, v, mask) -> Shape:
+    _check_qkv(q, k, v, mask)
+    B, Hq, L, E = q.shape
+    _, Hkv, S, _ = k.shape
     Ev = v.shape[3]
-    mb, mh = 1, 1
-    if mask is not None:
-        if mask.dim() != 4:
-            raise ValueError("mask must be 4-D [B|1, Hq|1, L, S]")
-        mb, mh = mask.shape[0], mask.shape[1]
+    mb, mh = (1, 1) if mask is None else (mask.shape[0], mask.shape[1])
     return Shape(B, Hq, Hkv, L, S, E, Ev, _dtype_code(q), mb, mh)
 
 
 def _check_tensors(*ts):
+    """Every tensor given is contiguous and on the first one's CUDA device."""
+    dev = None
     for t in ts:
         if t is None:
             continue
@@ -200,6 +238,20 @@ def _check_tensors(*ts):
             raise ValueError("tensors must be on a CUDA device")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous (BHSD)")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors must be on one device: {dev} and {t.device}")
+
+
+def _band_tensors(band):
+    return (None, None) if band is None else (band.seq_len_q, band.seq_len_kv)
+
+
+def _on_device(t):
+    """Makes t's device current for the call, so the library launches there and on its stream."""
+    import torch
+    return torch.cuda.device(t.device) if t.is_cuda else contextlib.nullcontext()
 
 
 def _ptr(t):
@@ -251,9 +303,18 @@ def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=Fal
     backward must get the same one).
     """
     import torch
-    lib = load_library()
-    _check_tensors(q, k, v, mask)
     shp = _shape(q, k, v, mask)
+    B, Hq, L, _ = q.shape
+    _expect(out, "out", (B, Hq, L, v.shape[3]), q.dtype)
+    _expect(lse, "lse", (B, Hq, L), torch.float32)
+    _check_tensors(q, k, v, mask, out, lse, workspace, *_band_tensors(band))
+    with _on_device(q):
+        return _forward(shp, q, k, v, mask, scale, is_causal, enable_gqa, out, lse, workspace, stream, band, dropout)
+
+
+def _forward(shp, q, k, v, mask, scale, is_causal, enable_gqa, out, lse, workspace, stream, band, dropout):
+    import torch
+    lib = load_library()
     B, Hq, L, _ = q.shape
     if out is None:
         out = torch.empty(B, Hq, L, v.shape[3], dtype=q.dtype, device=q.device)
@@ -266,7 +327,7 @@ def sdpa_forward(q, k, v, mask=None, scale=None, is_causal=False, enable_gqa=Fal
     if band is None and dropout is not None:
         band = Band(right_bound=0 if is_causal else None)
     if band is not None:
-        opts = band.options(dropout)
+        opts = band.options(dropout, batch=B)
         st = lib.sdpa_forward_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(mask),
                                    _scale(scale), int(bool(enable_gqa)), _ptr(out), _ptr(lse), _ptr(workspace), wsb,
                                    _stream(stream))
@@ -283,9 +344,24 @@ def sdpa_backward(q, k, v, o, dO, lse, mask=None, scale=None, is_causal=False, e
                   dq=None, dk=None, dv=None, workspace=None, stream=None, band=None, dropout=None):
     """dQ, dK, dV of sum(O * dO); o and lse are the forward's outputs (same band)."""
     import torch
-    lib = load_library()
-    _check_tensors(q, k, v, o, dO, lse, mask)
     shp = _shape(q, k, v, mask)
+    B, Hq, L, _ = q.shape
+    _expect(o, "o", (B, Hq, L, v.shape[3]), q.dtype)
+    _expect(dO, "dO", (B, Hq, L, v.shape[3]), q.dtype)
+    _expect(lse, "lse", (B, Hq, L), torch.float32)
+    _expect(dq, "dq", q.shape, q.dtype)
+    _expect(dk, "dk", k.shape, q.dtype)
+    _expect(dv, "dv", v.shape, q.dtype)
+    _check_tensors(q, k, v, o, dO, lse, mask, dq, dk, dv, workspace, *_band_tensors(band))
+    with _on_device(q):
+        return _backward(shp, q, k, v, o, dO, lse, mask, scale, is_causal, enable_gqa, dq, dk, dv, workspace,
+                         stream, band, dropout)
+
+
+def _backward(shp, q, k, v, o, dO, lse, mask, scale, is_causal, enable_gqa, dq, dk, dv, workspace, stream, band,
+              dropout):
+    import torch
+    lib = load_library()
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -295,7 +371,7 @@ def sdpa_backward(q, k, v, o, dO, lse, mask=None, scale=None, is_causal=False, e
     if band is None and dropout is not None:
         band = Band(right_bound=0 if is_causal else None)
     if band is not None:
-        opts = band.options(dropout)
+        opts = band.options(dropout, batch=q.shape[0])
         st = lib.sdpa_backward_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                     _ptr(dO), _ptr(lse), _ptr(mask), _scale(scale), int(bool(enable_gqa)), _ptr(dq),
                                     _ptr(dk), _ptr(dv), _ptr(workspace), wsb, _stream(stream))
@@ -312,9 +388,18 @@ def sdpa_decode(q, k, v, mask=None, scale=None, enable_gqa=False, num_splits=0,
                 out=None, lse=None, workspace=None, stream=None, band=None):
     """Split-KV decode forward (bf16): same outputs as sdpa_forward (band: sdpa_decode_opts)."""
     import torch
-    lib = load_library()
-    _check_tensors(q, k, v, mask)
     shp = _shape(q, k, v, mask)
+    B, Hq, L, _ = q.shape
+    _expect(out, "out", (B, Hq, L, v.shape[3]), q.dtype)
+    _expect(lse, "lse", (B, Hq, L), torch.float32)
+    _check_tensors(q, k, v, mask, out, lse, workspace, *_band_tensors(band))
+    with _on_device(q):
+        return _decode(shp, q, k, v, mask, scale, enable_gqa, num_splits, out, lse, workspace, stream, band)
+
+
+def _decode(shp, q, k, v, mask, scale, enable_gqa, num_splits, out, lse, workspace, stream, band):
+    import torch
+    lib = load_library()
     B, Hq, L, _ = q.shape
     if out is None:
         out = torch.empty(B, Hq, L, v.shape[3], dtype=q.dtype, device=q.device)
@@ -324,7 +409,7 @@ def sdpa_decode(q, k, v, mask=None, scale=None, enable_gqa=False, num_splits=0,
         workspace = _workspace(lib.sdpa_decode_workspace_bytes(ctypes.byref(shp), int(num_splits)), q.device)
     wsb = workspace.numel() * workspace.element_size()
     if band is not None:
-        opts = band.options()
+        opts = band.options(batch=B)
         st = lib.sdpa_decode_opts(ctypes.byref(shp), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(mask),
                                   _scale(scale), int(bool(enable_gqa)), int(num_splits), _ptr(out), _ptr(lse),
                                   _ptr(workspace), wsb, _stream(stream))
@@ -346,30 +431,39 @@ def sdpa_decode_paged(q, k_container, v_container, page_table_k, page_table_v, S
     carries seq_len_kv (each sequence's cache length).
     """
     import torch
-    lib = load_library()
-    _check_tensors(q, k_container, v_container, mask, page_table_k, page_table_v)
+    if q.dim() != 4 or k_container.dim() != 4 or v_container.dim() != 4:
+        raise ValueError("q and the containers must be 4-D")
+    B, Hq, L, E = q.shape
+    Hkv, Ev = k_container.shape[1], v_container.shape[3]
+    _expect(k_container, "k_container", (k_container.shape[0], Hkv, k_container.shape[2], E), q.dtype)
+    _expect(v_container, "v_container", (v_container.shape[0], Hkv, v_container.shape[2], Ev), q.dtype)
     for t in (page_table_k, page_table_v):
-        if t.dtype != torch.int32 or t.dim() != 2 or t.shape[0] != q.shape[0]:
+        if t.dtype != torch.int32 or t.dim() != 2 or t.shape[0] != B:
             raise ValueError("page tables must be int32 [B, max_blocks]")
     if page_table_k.shape != page_table_v.shape:
         raise ValueError("page tables must have the same shape")
-    B, Hq, L, E = q.shape
-    Hkv, Ev = k_container.shape[1], v_container.shape[3]
+    _check_mask(mask, L, int(S))
+    _expect(out, "out", (B, Hq, L, Ev), q.dtype)
+    _expect(lse, "lse", (B, Hq, L), torch.float32)
+    _check_tensors(q, k_container, v_container, mask, page_table_k, page_table_v, out, lse, workspace,
+                   *_band_tensors(band))
     mb, mh = (1, 1) if mask is None else (mask.shape[0], mask.shape[1])
     shp = Shape(B, Hq, Hkv, L, int(S), E, Ev, _dtype_code(q), mb, mh)
     paged = PagedKV(_ptr(page_table_k), _ptr(page_table_v), k_container.shape[2], v_container.shape[2],
                     page_table_k.shape[1], k_container.shape[0], v_container.shape[0])
-    opts = (band or Band()).options()
-    if out is None:
-        out = torch.empty(B, Hq, L, Ev, dtype=q.dtype, device=q.device)
-    if lse is None:
-        lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
-    if workspace is None:
-        workspace = _workspace(lib.sdpa_decode_workspace_bytes(ctypes.byref(shp), int(num_splits)), q.device)
-    st = lib.sdpa_decode_paged(ctypes.byref(shp), ctypes.byref(opts), ctypes.byref(paged), _ptr(q),
-                               _ptr(k_container), _ptr(v_container), _ptr(mask), _scale(scale), int(bool(enable_gqa)),
-                               int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream))
+    opts = (band or Band()).options(batch=B)
+    with _on_device(q):
+        lib = load_library()
+        if out is None:
+            out = torch.empty(B, Hq, L, Ev, dtype=q.dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = _workspace(lib.sdpa_decode_workspace_bytes(ctypes.byref(shp), int(num_splits)), q.device)
+        st = lib.sdpa_decode_paged(ctypes.byref(shp), ctypes.byref(opts), ctypes.byref(paged), _ptr(q),
+                                   _ptr(k_container), _ptr(v_container), _ptr(mask), _scale(scale),
+                                   int(bool(enable_gqa)), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(st, "sdpa_decode_paged")
     return out, lse
 
@@ -382,10 +476,7 @@ def last_device_status() -> int:
 def selftest_wait_timeout(stream=None) -> None:
     """Runs the failure-path self-test kernel (a bounded wait that nothing satisfies: it gives
     up after about a second and records a timeout); read last_device_status() afterwards."""
-    import torch
-    lib = load_library()
-    st = ctypes.c_void_p(stream if stream is not None else torch.cuda.current_stream().cuda_stream)
-    _raise(lib.sdpa_selftest_wait_timeout(st), "sdpa_selftest_wait_timeout")
+    _raise(load_library().sdpa_selftest_wait_timeout(_stream(stream)), "sdpa_selftest_wait_timeout")
 
 
 def default_scale(E: int) -> float:

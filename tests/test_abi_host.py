@@ -212,3 +212,74 @@ def test_dropout_options_are_checked(lib):
     o = sdpa.Options(None, None, 1, 0, 0, 0.1, 1, 0)   # the decode takes no dropout
     assert lib.sdpa_decode_opts(ctypes.byref(dshp), ctypes.byref(o), P(FAKE), P(FAKE), P(FAKE), None, float("nan"), 0,
                                 0, P(FAKE), P(FAKE), P(FAKE), 1 << 30, None) == INVALID
+
+
+def test_binding_checks_tensor_shapes_before_launching():
+    """The C ABI sees one shape; every tensor that disagrees with it is refused by the binding
+    (ValueError) before the library is loaded, so no kernel can run past a buffer."""
+    torch = pytest.importorskip("torch")
+    bf, f32 = torch.bfloat16, torch.float32
+    B, Hq, Hkv, L, S, E = 2, 4, 2, 8, 24, 16
+
+    def t(*shape, dtype=bf):
+        return torch.zeros(*shape, dtype=dtype)
+    q, k, v = t(B, Hq, L, E), t(B, Hkv, S, E), t(B, Hkv, S, E)
+    o, dO, lse = t(B, Hq, L, E), t(B, Hq, L, E), t(B, Hq, L, dtype=f32)
+    bad_forward = [
+        dict(k=t(B, Hkv, S, E + 16)),            # K width differs from Q's
+        dict(v=t(B, Hkv, S + 1, E)),             # V length differs from K's
+        dict(v=t(B, Hkv + 1, S, E)),
+        dict(k=t(B, Hkv, S, E, dtype=f32)),      # mixed dtypes
+        dict(mask=t(1, 1, L, S + 4, dtype=f32)),  # mask wider than S
+        dict(mask=t(1, 1, L - 1, S, dtype=f32)),
+        dict(mask=t(1, 1, L, S)),                # mask not fp32
+        dict(out=t(B, Hq, L + 1, E)),
+        dict(out=t(B, Hq, L, E, dtype=f32)),
+        dict(lse=t(B, Hq, L)),                   # lse not fp32
+        dict(lse=t(B, Hq, L + 1, dtype=f32)),
+    ]
+    for bad in bad_forward:
+        args = dict(q=q, k=k, v=v, mask=None, out=None, lse=None)
+        args.update(bad)
+        with pytest.raises(ValueError, match="must have shape|must be torch"):
+            sdpa.sdpa_forward(args["q"], args["k"], args["v"], args["mask"], out=args["out"], lse=args["lse"],
+                              enable_gqa=True)
+    for name, bad in (("o", t(B, Hq, L, E + 16)), ("dO", t(B, Hq, L - 1, E)), ("lse", t(B, Hq, L)),
+                      ("dq", t(B, Hq, L, E, dtype=f32)), ("dk", t(B, Hq, S, E)), ("dv", t(B, Hkv, S - 1, E))):
+        args = dict(o=o, dO=dO, lse=lse, dq=None, dk=None, dv=None)
+        args[name] = bad
+        with pytest.raises(ValueError, match="must have shape|must be torch"):
+            sdpa.sdpa_backward(q, k, v, args["o"], args["dO"], args["lse"], enable_gqa=True, dq=args["dq"],
+                               dk=args["dk"], dv=args["dv"])
+    qd = t(B, Hq, 1, E)
+    with pytest.raises(ValueError, match="must have shape"):
+        sdpa.sdpa_decode(qd, k, t(B, Hkv, S - 8, E), enable_gqa=True)
+    # consistent shapes get as far as the device check (host tensors are refused, never passed on)
+    with pytest.raises(ValueError, match="CUDA device"):
+        sdpa.sdpa_forward(q, k, v, t(1, 1, L, S, dtype=f32), enable_gqa=True)
+    with pytest.raises(ValueError, match="CUDA device"):
+        sdpa.sdpa_backward(q, k, v, o, dO, lse, enable_gqa=True)
+
+
+def test_binding_checks_paged_and_band_shapes():
+    torch = pytest.importorskip("torch")
+    bf = torch.bfloat16
+    B, Hq, Hkv, E, bs = 2, 4, 2, 16, 16
+    q = torch.zeros(B, Hq, 1, E, dtype=bf)
+    kc, vc = torch.zeros(10, Hkv, bs, E, dtype=bf), torch.zeros(10, Hkv, bs, E, dtype=bf)
+    pt = torch.zeros(B, 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="must have shape"):
+        sdpa.sdpa_decode_paged(q, torch.zeros(10, Hkv, bs, E + 16, dtype=bf), vc, pt, pt, 64, enable_gqa=True)
+    with pytest.raises(ValueError, match="must have shape"):
+        sdpa.sdpa_decode_paged(q, kc, torch.zeros(10, Hkv + 1, bs, E, dtype=bf), pt, pt, 64, enable_gqa=True)
+    with pytest.raises(ValueError, match="page tables"):
+        sdpa.sdpa_decode_paged(q, kc, vc, torch.zeros(B + 1, 4, dtype=torch.int32), pt, 64, enable_gqa=True)
+    with pytest.raises(ValueError, match="must have shape"):
+        sdpa.sdpa_decode_paged(q, kc, vc, pt, pt, 64, mask=torch.zeros(1, 1, 1, 63), enable_gqa=True)
+    with pytest.raises(ValueError, match="CUDA device"):
+        sdpa.sdpa_decode_paged(q, kc, vc, pt, pt, 64, enable_gqa=True)
+    # padding lengths: exactly B of them
+    with pytest.raises(ValueError, match="B = 2 lengths"):
+        sdpa.Band(seq_len_kv=torch.zeros(3, dtype=torch.int32)).options(batch=2)
+    with pytest.raises(ValueError, match="B = 2 lengths"):
+        sdpa.Band(seq_len_q=torch.zeros(1, 2, dtype=torch.int32)).options(batch=2)
