@@ -70,10 +70,23 @@ sdpa_status check_shape(const sdpa_shape* s, int enable_gqa, bool has_mask, Chec
     if (!(s->mask_b == 1 || s->mask_b == s->B) || !(s->mask_h == 1 || s->mask_h == s->Hq))
       return SDPA_ERR_INVALID_ARG;
   }
-  // sizes the kernels index with 32-bit row counters and grid dimensions
-  if (s->B * s->Hq > INT_MAX || s->L > INT_MAX / 2 || s->S > INT_MAX / 2 || s->B * s->Hkv > 65535 * 64)
+  // sizes the kernels index with 32-bit row counters and grid dimensions; each
+  // dimension is bounded before any product of them is formed
+  if (s->B > INT_MAX || s->Hq > INT_MAX || s->Hkv > INT_MAX || s->L > INT_MAX / 2 || s->S > INT_MAX / 2)
     return SDPA_ERR_UNSUPPORTED;
   if (s->E > 128 || s->Ev > 128) return SDPA_ERR_UNSUPPORTED;
+  if (s->B * s->Hq > INT_MAX || s->B * s->Hkv > 65535 * 64) return SDPA_ERR_UNSUPPORTED;
+  // element counts of every tensor and workspace stay below 2^56, so no byte count wraps
+  {
+    const double kMaxElems = 72057594037927936.0;   // 2^56
+    const double rows_q = static_cast<double>(s->B) * static_cast<double>(s->Hq) * static_cast<double>(s->L);
+    const double rows_kv = static_cast<double>(s->B) * static_cast<double>(s->Hkv) * static_cast<double>(s->S);
+    const double mask_elems =
+        has_mask ? static_cast<double>(s->mask_b) * s->mask_h * static_cast<double>(s->L) * static_cast<double>(s->S)
+                 : 0.0;
+    if (rows_q * 128.0 > kMaxElems || rows_kv * 128.0 > kMaxElems || mask_elems > kMaxElems)
+      return SDPA_ERR_UNSUPPORTED;
+  }
   if (s->dtype == SDPA_BF16 && (s->E % 8 != 0 || s->Ev % 8 != 0)) return SDPA_ERR_UNSUPPORTED;
   c->B = static_cast<int>(s->B);
   c->Hq = static_cast<int>(s->Hq);
@@ -395,7 +408,7 @@ sdpa_status check_paged(const sdpa_paged_kv* pg, const Checked& c) {
   const long long need_v = (static_cast<long long>(c.S) + pg->block_size_v - 1) / pg->block_size_v;
   if (pg->max_blocks < need_k || pg->max_blocks < need_v) return SDPA_ERR_INVALID_ARG;
   for (long long nb : {pg->num_blocks_k, pg->num_blocks_v})
-    if (nb < 1 || (nb + 1) * c.Hkv > INT_MAX) return SDPA_ERR_INVALID_ARG;
+    if (nb < 1 || nb > INT_MAX || (nb + 1) * c.Hkv > INT_MAX) return SDPA_ERR_INVALID_ARG;
   return SDPA_OK;
 }
 

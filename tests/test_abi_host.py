@@ -98,6 +98,14 @@ def test_forward_rejects_null_and_misaligned(lib):
 def test_forward_rejects_unsupported_sizes(lib):
     assert _fwd(lib, _shape(E=256, Ev=256)) == UNSUPPORTED
     assert _fwd(lib, _shape(E=60)) == UNSUPPORTED          # bf16 widths must be multiples of 8
+    # extents past the kernels' 32-bit counters, including ones whose products would overflow int64
+    assert _fwd(lib, _shape(B=1 << 40)) == UNSUPPORTED
+    assert _fwd(lib, _shape(B=1 << 62, Hq=1 << 62, Hkv=1 << 62)) == UNSUPPORTED
+    assert _fwd(lib, _shape(L=1 << 31)) == UNSUPPORTED
+    # tensors of 2^56 elements or more: q of 2^59 rows, then a mask of 2^64 elements
+    assert _fwd(lib, _shape(B=1 << 20, Hq=1 << 10, Hkv=1, L=1 << 29), gqa=1) == UNSUPPORTED
+    big = (1 << 30) - 1
+    assert _fwd(lib, _shape(B=4, Hq=4, Hkv=4, L=big, S=big, mb=4, mh=4), mask=FAKE) == UNSUPPORTED
 
 
 def test_backward_rejects_small_workspace(lib):
@@ -196,7 +204,7 @@ def test_decode_paged_rejects_bad_tables(lib):
     good = dict(page_table_k=FAKE, page_table_v=FAKE, block_size_k=16, block_size_v=16, max_blocks=7,
                 num_blocks_k=20, num_blocks_v=20)
     for bad in (dict(block_size_k=12), dict(block_size_v=4), dict(max_blocks=6), dict(page_table_k=FAKE + 2),
-                dict(page_table_v=None), dict(num_blocks_k=0)):
+                dict(page_table_v=None), dict(num_blocks_k=0), dict(num_blocks_v=1 << 62)):
         pg = sdpa.PagedKV(**{**good, **bad})
         assert call(ctypes.byref(pg)) == INVALID, bad
 
