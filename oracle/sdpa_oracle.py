@@ -453,34 +453,45 @@ def ref_backward_rows(q, k, v, dO, b, h, rows, mask=None, scale=None, is_causal=
     return _dq(dS, kh, alpha)
 
 
-def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False, band=None):
+def ref_group(q, k, v, dO, b, kv, mask=None, scale=None, is_causal=False, band=None, dropout=None):
     """Forward and backward of the G query heads sharing KV head (b, kv).
 
     Returns (O [G,L,Ev], LSE [G,L], dQ [G,L,E], dK [S,E], dV [S,Ev]) for
-    sampled checks of large runs: one KV group is a closed sub-problem.
+    sampled checks of large runs: one KV group is a closed sub-problem (the
+    heads are independent, course chapter section 2.1, and dK, dV of a KV head
+    sum only its own group's terms, section 2.3).  Each head keeps its index
+    (b, h) in the whole problem, so its padding lengths and its dropout mask
+    (section 2.5) are the ones the full call draws.
     """
-    G = q.shape[1] // k.shape[1]
-    sl = slice(kv * G, (kv + 1) * G)
-    qg = q[b:b + 1, sl]
-    kg = k[b:b + 1, kv:kv + 1]
-    vg = v[b:b + 1, kv:kv + 1]
-    dOg = dO[b:b + 1, sl] if dO is not None else None
-    mg = None
-    if mask is not None:
-        mb = min(b, mask.shape[0] - 1)
-        mg = mask[mb:mb + 1]
-        if mask.shape[1] != 1:
-            mg = mg[:, sl]
-    bg = None
-    if band is not None:   # the one batch of the group, with its own lengths
-        bg = Band(None if band.seq_len_q is None else [band.seq_len_q[b]],
-                  None if band.seq_len_kv is None else [band.seq_len_kv[b]],
-                  band.alignment, band.right_bound, band.left_bound)
-    O, LSE = ref_forward(qg, kg, vg, mg, scale, is_causal, enable_gqa=True, band=bg)
-    out = [O[0], LSE[0]]
+    Hq, Hkv = q.shape[1], k.shape[1]
+    G = Hq // Hkv
+    L, S, E = q.shape[2], k.shape[2], q.shape[3]
+    alpha = _alpha(scale, E)
+    kh, vh = _as64(k[b, kv]), _as64(v[b, kv])
+    mg = None if mask is None else _as64(mask[min(b, mask.shape[0] - 1)])      # [mask_h, L, S]
+    O, LSE, dQ = [], [], []
+    dK, dV = np.zeros((S, E)), np.zeros((S, vh.shape[1]))
+    for h in range(kv * G, (kv + 1) * G):
+        bias = np.zeros((L, S))
+        if mg is not None:
+            bias = bias + mg[min(h, mg.shape[0] - 1)]
+        if is_causal:
+            bias = bias + causal_bias(L, S)
+        if band is not None:
+            bias = bias + band_bias(L, S, band, b)
+        m = _dropout_m(dropout, b, h, Hq, L, S)
+        qh = _as64(q[b, h])
+        o, lse, P = _head_forward(qh, kh, vh, bias, alpha, m)
+        O.append(o)
+        LSE.append(lse)
+        if dO is not None:
+            dq, dk, dv, _ = _head_backward(qh, kh, vh, P, o, _as64(dO[b, h]), alpha, m)
+            dQ.append(dq)
+            dK += dk
+            dV += dv
+    out = [np.stack(O), np.stack(LSE)]
     if dO is not None:
-        dQ, dK, dV = ref_backward(qg, kg, vg, dOg, mg, scale, is_causal, enable_gqa=True, band=bg)
-        out += [dQ[0], dK[0, 0], dV[0, 0]]
+        out += [np.stack(dQ), dK, dV]
     return tuple(out)
 
 

@@ -1,5 +1,9 @@
 """Full-size workloads, in the launch configuration the benchmark times.
 
+The benchmark's workloads include the padding-length, sliding-window and dropout
+variants, which run here with the same lengths, window and (seed 0, offset 0)
+dropout as in the benchmark.
+
 Each workload runs whole on the GPU; the float64 oracle then recomputes
 sampled closed sub-problems (whole KV groups: the Hq/Hkv query heads sharing a
 KV head, with all their keys and queries) and every output of those groups is
@@ -44,10 +48,21 @@ def run_workload(name, groups):
     q, k, v, dO, mask = workloads.make_inputs(w, seed=0, with_grad="bwd" in w.phases)
     dev = [None if x is None else x.cuda() for x in (q, k, v, dO, mask)]
     qd, kd, vd, dOd, md = dev
-    o, lse = sdpa.sdpa_forward(qd, kd, vd, md, w.scale, w.is_causal, w.enable_gqa)
+    spec = workloads.make_band(w, seed=0)
+    band = ob = None
+    if spec is not None:
+        lens = [None if spec[n] is None else torch.tensor(spec[n], dtype=torch.int32, device="cuda")
+                for n in ("seq_len_q", "seq_len_kv")]
+        band = sdpa.Band(*lens, spec["alignment"], spec["right_bound"], spec["left_bound"])
+        ob = oracle.Band(spec["seq_len_q"], spec["seq_len_kv"], spec["alignment"], spec["right_bound"],
+                         spec["left_bound"])
+    drop = sdpa.Dropout(w.dropout, 0, 0) if w.dropout > 0 else None
+    odrop = oracle.Dropout(w.dropout, 0, 0) if w.dropout > 0 else None
+    o, lse = sdpa.sdpa_forward(qd, kd, vd, md, w.scale, w.is_causal, w.enable_gqa, band=band, dropout=drop)
     grads = None
     if "bwd" in w.phases:
-        grads = sdpa.sdpa_backward(qd, kd, vd, o, dOd, lse, md, w.scale, w.is_causal, w.enable_gqa)
+        grads = sdpa.sdpa_backward(qd, kd, vd, o, dOd, lse, md, w.scale, w.is_causal, w.enable_gqa, band=band,
+                                   dropout=drop)
     torch.cuda.synchronize()
     assert sdpa.last_device_status() == 0
     assert torch.isfinite(o).all()
@@ -57,7 +72,7 @@ def run_workload(name, groups):
     G = w.Hq // w.Hkv
     for b, kv in groups:
         sl = slice(kv * G, (kv + 1) * G)
-        out = oracle.ref_group(q, k, v, dO, b, kv, mask, w.scale, w.is_causal)
+        out = oracle.ref_group(q, k, v, dO, b, kv, mask, w.scale, w.is_causal, band=ob, dropout=odrop)
         ref_o, ref_lse = out[0], out[1]
         lg = lse[b, sl].double().cpu().numpy()
         dead = np.isneginf(ref_lse)
@@ -100,3 +115,20 @@ def test_padded_mask_e128():
 
 def test_gqa_decode_s32k():
     run_workload("gqa_decode_s32k", [(0, 0), (15, 7)])
+
+
+def test_padded_seqlen_e128():
+    """Padding lengths instead of a mask: keys at or past a sequence's length get exact zero dK, dV."""
+    w, q, k, v, mask, o, lse, grads = run_workload("padded_seqlen_e128", [(0, 0), (5, 9), (7, 15)])
+    lens = workloads.make_band(w, seed=0)["seq_len_kv"]
+    dq, dk, dv = grads
+    for b, n in enumerate(lens):
+        assert int(torch.count_nonzero(dk[b, :, n:])) == 0 and int(torch.count_nonzero(dv[b, :, n:])) == 0
+
+
+def test_gqa_swa_e128():
+    run_workload("gqa_swa_e128", [(0, 0), (1, 7)])
+
+
+def test_gqa_causal_dropout_e128():
+    run_workload("gqa_causal_dropout_e128", [(0, 0), (1, 5)])

@@ -445,6 +445,20 @@ def test_group_and_rows_helpers_match_full():
     dQb = oracle.ref_backward(q, k, v, dO, mask, 0.5, False, True, band=band)[0]
     dQrb = oracle.ref_backward_rows(q, k, v, dO, 0, 1, [1, 2, 5], mask, 0.5, False, True, band=band)
     np.testing.assert_allclose(dQrb, dQb[0, 1, [1, 2, 5]], atol=1e-13)
+    # the group restriction keeps each head's padding lengths and dropout mask
+    drop = oracle.Dropout(0.3, seed=12345, offset=7)
+    Od, Ld = oracle.ref_forward(q, k, v, mask, 0.5, False, True, band=band, dropout=drop)
+    dQd, dKd, dVd = oracle.ref_backward(q, k, v, dO, mask, 0.5, False, True, band=band, dropout=drop)
+    for b, kv in ((0, 0), (1, 1)):
+        Og, Lg, dQg, dKg, dVg = oracle.ref_group(q, k, v, dO, b, kv, mask, 0.5, False, band=band, dropout=drop)
+        hs = slice(2 * kv, 2 * kv + 2)
+        np.testing.assert_allclose(Og, Od[b, hs], atol=1e-13)
+        np.testing.assert_allclose(Lg, Ld[b, hs], atol=1e-13)
+        np.testing.assert_allclose(dQg, dQd[b, hs], atol=1e-13)
+        np.testing.assert_allclose(dKg, dKd[b, kv], atol=1e-13)
+        np.testing.assert_allclose(dVg, dVd[b, kv], atol=1e-13)
+    # and the dropout is live there: without it the group's O differs
+    assert np.abs(oracle.ref_group(q, k, v, None, 1, 1, mask, 0.5, False, band=band)[0] - Od[1, 2:4]).max() > 1e-3
 
 
 def test_repeated_keys_equal_log_multiplicity_bias():
