@@ -79,3 +79,36 @@ def test_paged_decode(case):
     torch.cuda.synchronize()
     assert torch.equal(o, od) and torch.equal(lse, lsed)
     assert sdpa.last_device_status() == 0
+
+
+def test_paged_decode_full_size():
+    """The 32k-key GQA decode workload (B = 16, Hq = 32, Hkv = 8, S = 32768) with its caches cut into
+    64-key blocks shuffled across one container: bit-identical to the dense decode, and sampled KV
+    groups match the oracle."""
+    import workloads
+    w = workloads.get("gqa_decode_s32k")
+    q, k, v, _, _ = workloads.make_inputs(w, seed=0, with_grad=False)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    bs = 64
+    nb = w.S // bs
+    perm = torch.randperm(w.B * nb, device="cuda", generator=torch.Generator(device="cuda").manual_seed(5))
+
+    def container(x):   # block i of sequence b lands at perm[b * nb + i]
+        B, H, S, D = x.shape
+        blocks = x.reshape(B, H, nb, bs, D).permute(0, 2, 1, 3, 4).reshape(B * nb, H, bs, D)
+        c = torch.empty_like(blocks)
+        c[perm] = blocks
+        return c
+    table = perm.reshape(w.B, nb).to(torch.int32).contiguous()
+    o, lse = sdpa.sdpa_decode_paged(qd, container(kd), container(vd), table, table, w.S, None, w.scale, True, 0)
+    od, lsed = sdpa.sdpa_decode(qd, kd, vd, None, w.scale, True, 0)
+    torch.cuda.synchronize()
+    assert sdpa.last_device_status() == 0
+    assert torch.equal(o, od) and torch.equal(lse, lsed)
+    G = w.Hq // w.Hkv
+    for b, kv in ((0, 0), (9, 3), (15, 7)):
+        ref_o, ref_lse = oracle.ref_group(q, k, v, None, b, kv, None, w.scale, False)
+        sl = slice(kv * G, (kv + 1) * G)
+        got = o[b, sl].float().cpu().double().numpy()
+        assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= 5e-3
+        assert np.abs(lse[b, sl].cpu().double().numpy() - ref_lse).max() <= 1e-3
