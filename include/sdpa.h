@@ -52,7 +52,11 @@
  * Supported sizes: B, Hq, Hkv, L, S >= 1.  fp32: 1 <= E, Ev <= 128.  bf16:
  * E and Ev multiples of 8, at most 128 (the tensor-core prefill and backward
  * take E, Ev in {64, 128}; other bf16 widths run on the CUDA-core kernels).
- * Anything else -> SDPA_ERR_UNSUPPORTED.
+ * Extents: B, Hq, Hkv <= 2^31 - 1, B * Hq <= 2^31 - 1, L, S <= 2^30 - 1,
+ * B * Hkv <= 4,194,240, B * Hq * L and B * Hkv * S at most 2^49 rows, and
+ * at most 2^56 mask elements (each extent is bounded before any product is
+ * formed, so no size computation wraps).  Anything else ->
+ * SDPA_ERR_UNSUPPORTED.
  */
 #ifndef SDPA_GB300_H
 #define SDPA_GB300_H
