@@ -1,7 +1,7 @@
 """Float64 CPU oracle of scaled dot-product attention.
 
 TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
-benchmark's CPU-baseline leg, never by the library.
+benchmark's CPU legs (CPU baseline, reference arm), never by the library.
 """
 from .sdpa_oracle import (  # noqa: F401
     Band, Dropout, band_bias, causal_bias, default_scale, dropout_keep, gather_paged, philox4x32_10, ref_backward,

@@ -2,8 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY.  This module is the plain, slow, obviously correct
 definition that the CUDA library is checked against.  Only the test suite,
-the smoke check and the benchmark's CPU-baseline leg may import it; the
-library itself never does, and it shares no code with the CUDA path.
+the smoke check and the benchmark's CPU legs (its CPU baseline and its
+reference arm) may import it; the library itself never does, and it shares
+no code with the CUDA path.
 
 Everything is NumPy float64, one (batch, query head) problem at a time, in the
 order and notation of the course chapter "Scaled dot-product attention
@@ -48,7 +49,7 @@ Sources for each step (page title, section):
     page tables (B, ceil(S / bs)): "Attention" (cuDNN), Configurable Options
     (Paged attention, Offset calculation) and Tensors (Page Table K / V).
 
-Readings where the pages are silent (every one also listed in the design notes):
+Readings where the pages are silent:
   * a fully blocked row has LSE = -inf, O = 0, dQ = 0 and contributes nothing
     to dK/dV; padded query rows (i >= seq_len_q[b]) are such rows;
   * dropout uniforms (the pages fix the rule u >= p and name a Philox
