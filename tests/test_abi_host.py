@@ -291,3 +291,23 @@ def test_binding_checks_paged_and_band_shapes():
         sdpa.Band(seq_len_kv=torch.zeros(3, dtype=torch.int32)).options(batch=2)
     with pytest.raises(ValueError, match="B = 2 lengths"):
         sdpa.Band(seq_len_q=torch.zeros(1, 2, dtype=torch.int32)).options(batch=2)
+
+
+def test_library_and_oracle_share_nothing():
+    """The product path (package, kernels, header) never names or imports the oracle, and the
+    oracle never imports the package: the two sides of every parity check are independent."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "scaled_dot_product_sm_gb300")
+    product = [os.path.join(dp, f) for dp, _, fs in os.walk(pkg) for f in fs
+               if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp"))]
+    product += [os.path.join(root, "include", f) for f in os.listdir(os.path.join(root, "include"))]
+    assert len(product) > 5
+    for path in product:
+        with open(path, encoding="utf-8") as fh:
+            assert not re.search(r"\boracle\b", fh.read()), path
+    odir = os.path.join(root, "oracle")
+    for f in os.listdir(odir):
+        if f.endswith(".py"):
+            with open(os.path.join(odir, f), encoding="utf-8") as fh:
+                src = fh.read()
+            assert "scaled_dot_product_sm_gb300" not in src and "workloads" not in src, f
