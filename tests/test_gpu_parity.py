@@ -92,9 +92,12 @@ def check_backward(grads, refs, dead_rows, blocked, bf16):
 
 
 def run_case(B, Hq, Hkv, L, S, E, Ev, dtype, causal, mask_kind="none", mask_shape=None, full_rows=0,
-             scale=None, seed=0, backward=True, p_block=0.25):
+             scale=None, seed=0, backward=True, p_block=0.25, k_growth=0.0):
     q, k, v, dO, mask = random_inputs(B, Hq, Hkv, L, S, E, Ev, dtype, seed=seed, mask_shape=mask_shape,
                                       mask_kind=mask_kind, full_rows=full_rows, p_block=p_block)
+    if k_growth:   # key j scaled by 1 + k_growth * j / S: the scores grow along the keys
+        g = 1.0 + k_growth * torch.arange(S, dtype=torch.float32) / S
+        k = (k.float() * g[None, None, :, None]).to(dtype)
     gqa = Hq != Hkv
     bf16 = dtype == torch.bfloat16
     ref_o, ref_lse = oracle.ref_forward(q, k, v, mask, scale, causal, gqa)
@@ -111,6 +114,15 @@ def run_case(B, Hq, Hkv, L, S, E, Ev, dtype, causal, mask_kind="none", mask_shap
         check_backward((dq, dk, dv), refs, np.isneginf(ref_lse), blocked_keys(m64, causal, B, Hq, Hkv, L, S),
                        bf16)
     assert sdpa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_max_growing_across_key_tiles(causal):
+    """Scores that grow along the keys (key j scaled by 1 + 7 j / S, so a 128-key tile's row max
+    rises by about 2 natural-log units per tile): the running row max moves past the kernels'
+    rescale threshold (2^8 in the exponentials) several times per row, so O is rescaled and the
+    exponentials of those tiles are taken again with the new max."""
+    run_case(1, 4, 2, 700, 1000, 128, 128, torch.bfloat16, causal, seed=41, k_growth=7.0)
 
 
 # ----------------------------------------------------------------------------- fp32
