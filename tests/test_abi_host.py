@@ -311,3 +311,48 @@ def test_library_and_oracle_share_nothing():
             with open(os.path.join(odir, f), encoding="utf-8") as fh:
                 src = fh.read()
             assert "scaled_dot_product_sm_gb300" not in src and "workloads" not in src, f
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/sdpa.h compiles as strict C11, every declared entry point links against the
+    library, and a C caller gets INVALID_ARG back from calls without a shape (nothing reaches
+    the GPU)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    sdpa.build()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(sdpa.LIB_PATH)
+    names = sdpa.EXPORTS
+    src = tmp_path / "caller.c"
+    src.write_text("\n".join([
+        '#include "sdpa.h"',
+        "#include <stdio.h>",
+        "typedef void (*any_fn)(void);",
+        "static const any_fn entry_points[] = {" + ", ".join(f"(any_fn){n}" for n in names) + "};",
+        "int main(void) {",
+        "  if (sizeof(entry_points) / sizeof(entry_points[0]) != %d) return 2;" % len(names),
+        "  if (sdpa_forward(NULL, NULL, NULL, NULL, NULL, 0.0, 0, 0, NULL, NULL, NULL, 0, NULL)"
+        " != SDPA_ERR_INVALID_ARG) return 3;",
+        "  if (sdpa_backward(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0.0, 0, 0, NULL, NULL, NULL,"
+        " NULL, 0, NULL) != SDPA_ERR_INVALID_ARG) return 4;",
+        "  if (sdpa_decode(NULL, NULL, NULL, NULL, NULL, 0.0, 0, 0, NULL, NULL, NULL, 0, NULL)"
+        " != SDPA_ERR_INVALID_ARG) return 5;",
+        '  printf("%s\\n", sdpa_status_string(SDPA_ERR_INVALID_ARG));',
+        "  return 0;",
+        "}",
+    ]) + "\n")
+    exe = tmp_path / "caller"
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.join(root, "include"), str(src), "-o", str(exe), "-L", libdir, "-lsdpa_gb300",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    assert run.stdout.strip() == lib_status_string(1)
+
+
+def lib_status_string(code):
+    return sdpa.load_library().sdpa_status_string(code).decode()
