@@ -226,6 +226,24 @@ def pin_queries_independent():
     np.testing.assert_allclose(dK, dKp, atol=1e-12)
 
 
+def pin_batched_equals_per_item():
+    """Each batch item is its own problem (course chapter, section 2.1: the batch index only
+    selects inputs): a batch of three with a per-item mask gives, item by item, exactly what
+    each item gives alone."""
+    q, k, v, dO, mask = random_inputs(3, 4, 2, 5, 7, 3, 2, torch.float64, seed=13,
+                                      mask_kind="bias", mask_shape=(3, 4), p_block=0.2)
+    q, k, v, dO, mask = _np(q), _np(k), _np(v), _np(dO), _np(mask)
+    O, L = oracle.ref_forward(q, k, v, mask, 0.7, True, True)
+    grads = oracle.ref_backward(q, k, v, dO, mask, 0.7, True, True)
+    for b in range(3):
+        sl = slice(b, b + 1)
+        Ob, Lb = oracle.ref_forward(q[sl], k[sl], v[sl], mask[sl], 0.7, True, True)
+        np.testing.assert_allclose(O[sl], Ob, atol=1e-13)
+        np.testing.assert_allclose(L[sl], Lb, atol=1e-13)
+        for g, gb in zip(grads, oracle.ref_backward(q[sl], k[sl], v[sl], dO[sl], mask[sl], 0.7, True, True)):
+            np.testing.assert_allclose(g[sl], gb, atol=1e-13)
+
+
 def pin_gqa_is_repeat_interleave():
     """"Understanding PyTorch SDPA" section 4: GQA equals repeat_interleave of K/V; gradients sum over the group."""
     G, Hkv = 3, 2
@@ -328,7 +346,7 @@ def pin_torch_cross_check():
 PINS = [pin_hand_forward, pin_hand_backward, pin_gradcheck, pin_lse_is_log_normaliser,
         pin_rows_sum_to_one_and_blocked_zero, pin_fully_masked_row, pin_large_scores_one_hot,
         pin_dk_sums_to_zero, pin_D_identity, pin_key_permutation_equivariance,
-        pin_queries_independent, pin_gqa_is_repeat_interleave, pin_zero_scale_is_mean,
+        pin_queries_independent, pin_batched_equals_per_item, pin_gqa_is_repeat_interleave, pin_zero_scale_is_mean,
         pin_single_key, pin_causal_first_row, pin_default_scale_variance, pin_torch_cross_check]
 
 
@@ -374,6 +392,10 @@ def _m_minus_1e9(s, bias):
     return so.__dict__["_orig_masked_softmax"](s, np.where(np.isneginf(bias), -1e9, bias))
 
 
+def _m_mask_of_batch_zero(mask, b, h, L, S, is_causal, band=None):
+    return so.__dict__["_orig_head_bias"](mask, 0, h, L, S, is_causal, band)
+
+
 MUTANTS = {
     "s01_scale_1_over_d": ("default_scale", _m_scale_1_over_d),
     "s02_softmax_over_queries": ("_masked_softmax", _m_softmax_query_axis),
@@ -382,6 +404,7 @@ MUTANTS = {
     "s05_dk_without_transpose": ("_dk", _m_dk_no_transpose),
     "s06_dq_without_scale": ("_dq", _m_dq_no_scale),
     "s10_mask_with_minus_1e9": ("_masked_softmax", _m_minus_1e9),
+    "x01_mask_of_batch_zero": ("_head_bias", _m_mask_of_batch_zero),   # a broadcast-index slip
 }
 
 
@@ -389,6 +412,7 @@ MUTANTS = {
 def test_mutants_are_caught(name, monkeypatch):
     attr, fn = MUTANTS[name]
     monkeypatch.setitem(so.__dict__, "_orig_masked_softmax", so._masked_softmax)
+    monkeypatch.setitem(so.__dict__, "_orig_head_bias", so._head_bias)
     monkeypatch.setattr(so, attr, fn)
     failed = []
     for pin in PINS:
