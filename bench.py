@@ -43,6 +43,12 @@ METRIC = "SDPA fwd/bwd TFLOP/s and % of GB300 bf16 peak; decode HBM GB/s"
 MAIN = "gqa_causal_e128"
 DECODE = "gqa_decode_s32k"
 NOMINAL_BF16_TFLOPS = 2250.0   # dense bf16 tensor rate of the part (context beside the measured peak)
+# Dense bf16 tcgen05.mma rate of one SM, measured on GB300 with chains of M=128, N=256,
+# K=128 kind::f16 MMAs, one CTA per SM, timed with clock64: 8173-8182 flop per SM clock
+# (the 8192 of one 128x256x16 MMA per 128 clocks, less issue gaps).  The computed
+# peak is SMs x this rate x SM clock.
+TCGEN05_BF16_FLOP_PER_CLK_SM = 8182.0
+SUSTAIN_S = 2.0                # seconds of the same step run right after the timed loop, for clock samples
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 
@@ -119,7 +125,9 @@ def reduce_max(x, ws):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 200 ms while the block runs; mark() notes host times so that
+    summary() can keep only the samples taken inside a window (the loops under load)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -127,6 +135,12 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.marks = {}
+        self.rows = None
+
+    def mark(self, name):
+        import datetime
+        self.marks[name] = datetime.datetime.now()
 
     def __enter__(self):
         try:
@@ -149,29 +163,50 @@ class ClockSampler:
             except Exception:  # noqa: BLE001
                 self.proc.kill()
 
-    def summary(self):
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def _load(self):
+        if self.rows is not None:
+            return self.rows
+        import datetime
+        self.rows = []
         if self.proc is None or not self.path or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            return self.rows
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    row = {"ts": ts, "sm": float(parts[2]), "smax": float(parts[3])}
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
+                try:
+                    row["w"] = float(parts[4])
+                except ValueError:
+                    row["w"] = None
+                row["reasons"] = {n for n, v in zip(self.REASONS, parts[6:10]) if v.lower().startswith("active")}
+                self.rows.append(row)
         os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return self.rows
+
+    def summary(self, start=None, end=None):
+        """Median SM clock, max clock and throttle reasons of the samples between marks
+        `start` and `end` (all samples when not given)."""
+        rows = self._load()
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t0 = self.marks.get(start) if start else None
+        t1 = self.marks.get(end) if end else None
+        sel = [r for r in rows if (t0 is None or r["ts"] >= t0) and (t1 is None or r["ts"] <= t1)]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["no samples"]}
+        reasons = set().union(*(r["reasons"] for r in sel))
+        watts = [r["w"] for r in sel if r["w"] is not None]
+        return {"sm_mhz": statistics.median(r["sm"] for r in sel), "sm_max_mhz": max(r["smax"] for r in sel),
+                "sm_mhz_min": min(r["sm"] for r in sel), "samples": len(sel),
+                "power_w_median": statistics.median(watts) if watts else None, "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ helpers
@@ -216,6 +251,11 @@ def visible_pairs(w, spec) -> int:
         lo = np.zeros(Lb, np.int64) if spec["left_bound"] is None else np.maximum(0, diag - spec["left_bound"] + 1)
         total += int(np.maximum(0, hi - lo + 1).sum())
     return total * w.Hq
+
+
+def computed_peak_tflops(sms: int, mhz: float) -> float:
+    """Datasheet-style dense bf16 peak: SMs x measured tcgen05 flop per SM clock x clock."""
+    return sms * TCGEN05_BF16_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
 
 
 def fp32_alu_peak_tflops(sms: int, mhz: float) -> float:
@@ -289,6 +329,7 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.mark("timed_start")
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             evs[i][0].record(stream)
@@ -298,12 +339,32 @@ def run_ours(args, ws, rank, local):
                 bwd()
             evs[i][2].record(stream)
         torch.cuda.synchronize()
+        clk.mark("timed_end")
+        barrier(ws)
+        t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+        t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+        # The same step again, back to back for SUSTAIN_S seconds right after the timed loop
+        # (outside it), so that the 200 ms clock samples land under this load; its rate is
+        # reported beside the timed one.
+        n_sus = max(1, int(SUSTAIN_S * 1e3 / max(t_fwd + t_bwd + 0.05, 1e-3)))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(n_sus):
+            flush.fill_(i & 0xFF)
+            fwd()
+            if not fwd_only:
+                bwd()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        clk.mark("sustain_end")
     barrier(ws)
-    clocks = clk.summary()
-    t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    clocks = clk.summary("timed_start", "sustain_end")
+    clocks["samples_in_timed_loop"] = clk.summary("timed_start", "timed_end").get("samples", 0)
+    clocks["window"] = (f"the timed loop and {n_sus} more steps of the same work run back to back after it "
+                        f"({s0.elapsed_time(s1) / 1e3:.2f} s)")
     t_step = t_fwd + t_bwd
     t_step_max = reduce_max(t_step, ws)
+    sustained = {"steps": n_sus, "ms_per_step_incl_flush": round(s0.elapsed_time(s1) / n_sus, 4)}
     if spec is None:
         f_fwd, f_bwd = w.flops("fwd"), w.flops("bwd")
     else:
@@ -411,17 +472,32 @@ def run_ours(args, ws, rank, local):
     bwd_launches = 3   # tensor cores: row stats, main, dQ convert; CUDA cores: pre-pass, dQ, dK/dV
     fwd_launches = 1
     launches = args.steps * (fwd_launches + bwd_launches)
+    med_mhz = clocks.get("sm_mhz") or peaks["sm_max_mhz"]
+    cpeak_max = computed_peak_tflops(sms, peaks["sm_max_mhz"])
+    cpeak_med = computed_peak_tflops(sms, med_mhz)
+
+    def phase(ms, flops, kernel, nl):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"ms": round(ms, 4), "tflops": round(tf, 2),
+                "frac_of_computed_peak": round(tf / cpeak_max, 4),
+                "frac_of_computed_peak_at_median_clock": round(tf / cpeak_med, 4),
+                "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                "frac_of_2250_nominal": round(tf / NOMINAL_BF16_TFLOPS, 4),
+                "kcycles_at_median_clock": round(ms * med_mhz, 1),
+                "kernel": kernel, "launches_per_step": nl}
+
     phases = {
-        "fwd": {"ms": round(t_fwd, 4), "tflops": round(f_fwd / (t_fwd * 1e-3) / 1e12, 2),
-                "frac_of_bf16_peak": round(f_fwd / (t_fwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                "frac_of_2250_nominal": round(f_fwd / (t_fwd * 1e-3) / 1e12 / NOMINAL_BF16_TFLOPS, 4),
-                "kernel": "fwd_tc_kernel" if fwd_tc else "fwd_simt_kernel", "launches_per_step": fwd_launches},
-        "bwd": {"ms": round(t_bwd, 4), "tflops": round(f_bwd / (t_bwd * 1e-3) / 1e12, 2),
-                "frac_of_bf16_peak": round(f_bwd / (t_bwd * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                "frac_of_2250_nominal": round(f_bwd / (t_bwd * 1e-3) / 1e12 / NOMINAL_BF16_TFLOPS, 4),
-                "kernel": "bwd_tc_kernel" if bwd_tc else "bwd_dq_simt_kernel+bwd_dkdv_simt_kernel",
-                "launches_per_step": bwd_launches},
+        "fwd": phase(t_fwd, f_fwd, "fwd_tc_kernel" if fwd_tc else "fwd_simt_kernel", fwd_launches),
+        "bwd": phase(t_bwd, f_bwd, "bwd_tc_kernel" if bwd_tc else "bwd_dq_simt_kernel+bwd_dkdv_simt_kernel",
+                     bwd_launches),
     }
+    computed_peak = {
+        "tflops_at_max_clock": round(cpeak_max, 1), "tflops_at_median_clock": round(cpeak_med, 1),
+        "sms": sms, "flop_per_clk_per_sm": TCGEN05_BF16_FLOP_PER_CLK_SM, "max_mhz": peaks["sm_max_mhz"],
+        "median_mhz": med_mhz,
+        "how": "SMs x dense bf16 tcgen05.mma flop per SM clock (measured: chains of M=128, N=256 kind::f16 "
+               "MMAs, one CTA per SM, clock64) x SM clock (the part's maximum, and the median sampled under "
+               "this load)"}
     if t_fwd >= t_bwd and not fwd_tc:
         achieved = f_fwd / (t_fwd * 1e-3) / 1e12
         pk = fp32_alu_peak_tflops(sms, peaks["sm_max_mhz"])
@@ -455,6 +531,9 @@ def run_ours(args, ws, rank, local):
                     "peak_source": f"FFMA: {sms} SMs x 128 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                     "algorithmic_per_launch": f_bwd}
     roof["duration_ms"] = round(max(t_fwd, t_bwd), 4)
+    if roof["bound"] == "tensor":
+        roof["frac_of_computed_peak"] = round(roof["achieved"] / cpeak_max, 4)
+        roof["frac_of_computed_peak_at_median_clock"] = round(roof["achieved"] / cpeak_med, 4)
 
     # ---------------------------------------------------------- decode leg
     decode = None
@@ -480,23 +559,35 @@ def run_ours(args, ws, rank, local):
         barrier(ws)
         torch.cuda.synchronize()
         with ClockSampler(local) as dclk:
+            dclk.mark("timed_start")
             for i in range(args.steps):
                 dev_evs[i][0].record(stream)
                 dstep()
                 dev_evs[i][1].record(stream)
             torch.cuda.synchronize()
+            dclk.mark("timed_end")
+            t_dec1 = sum(a.elapsed_time(b) for a, b in dev_evs) / args.steps
+            for _ in range(max(1, int(SUSTAIN_S * 1e3 / max(t_dec1, 1e-3)))):   # clock samples under load
+                dstep()
+            torch.cuda.synchronize()
+            dclk.mark("sustain_end")
         barrier(ws)
-        t_dec = reduce_max(sum(a.elapsed_time(b) for a, b in dev_evs) / args.steps, ws)
+        t_dec = reduce_max(t_dec1, ws)
+        dclocks = dclk.summary("timed_start", "sustain_end")
+        dclocks["samples_in_timed_loop"] = dclk.summary("timed_start", "timed_end").get("samples", 0)
         kv_bytes = (kd.numel() + vd.numel()) * kd.element_size()
         io_bytes = kv_bytes + qd.numel() * 2 + od.numel() * 2 + lsed.numel() * 4
         gbps = job_rate(ws, io_bytes, t_dec, 1e9)
         decode = {"workload": DECODE, "ms": round(t_dec, 4), "gbps": round(gbps, 1),
-                  "frac_of_measured_hbm": round(gbps / ws / peaks["hbm_gbs"], 4),
                   "frac_of_8tbs_nominal": round(gbps / ws / 8000.0, 4),
+                  "frac_of_measured_hbm": round(gbps / ws / peaks["hbm_gbs"], 4),
+                  "denominators": "headline: the 8 TB/s nominal HBM3e rate; beside it the measured copy "
+                                  "(a read+write stream, which runs below what a read-only stream such as "
+                                  "this one reaches, so its fraction can pass 1)",
                   "algorithmic_bytes": io_bytes, "splits": nsplit, "launches_per_step": 2,
                   "kernels": ["decode_split_kernel", "decode_merge_kernel"],
                   "traffic": traffic_for("decode_split_kernel", ["decode.cu", "ptx.cuh", "common.cuh"]),
-                  "clocks": dclk.summary(),
+                  "clocks": dclocks,
                   "l2": "inputs (2.1 GB of K/V) larger than L2; no flush"}
         launches += args.steps * 2
         assert sdpa.last_device_status() == 0
@@ -542,7 +633,9 @@ def run_ours(args, ws, rank, local):
     # ---------------------------------------------------------- CPU baseline (oracle)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        cpu = cpu_oracle_sample(w, seconds_target=15.0)
+        cpu = cpu_oracle_groups(w, seconds_target=12.0)
+        if decode is not None:
+            decode["cpu_baseline"] = cpu_oracle_groups(workloads.get(DECODE), seconds_target=8.0)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -557,6 +650,8 @@ def run_ours(args, ws, rank, local):
                    "l2": "256 MiB flush between timed steps, outside the events",
                    "parallelism": f"replicas x{ws} (no exchange)"},
         "phases": phases,
+        "computed_peak": computed_peak,
+        "sustained": sustained,
         "roofline": roof,
         "decode": decode,
         "cpu_baseline": cpu,
@@ -587,66 +682,72 @@ def run_decode_only(args, ws, local, dev, peaks):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def _oracle_head_sample(w, nheads=1):
-    """One (batch 0) query head of the workload: inputs and nominal FLOPs of fwd+bwd on it."""
-    import torch
-
-    import workloads
-    q, k, v, dO, mask = workloads.make_inputs(w, seed=0)
+def group_work(w, spec, b):
+    """Algorithmic work of one KV group (the Hq/Hkv query heads of batch b sharing a KV head):
+    forward + backward FLOPs (4E + 10E per visible (query, key) pair), or for a forward-only
+    workload the bytes of K and V read once plus Q, O and LSE."""
     G = w.Hq // w.Hkv
-    qs, dOs = q[:1, :nheads], dO[:1, :nheads]
-    kv_heads = sorted({h // G for h in range(nheads)})
-    ks, vs = k[:1, kv_heads], v[:1, kv_heads]
-    ms = None if mask is None else mask[:1]
-    sub = w.with_(B=1, Hq=nheads, Hkv=len(kv_heads))
-    spec = workloads.make_band(w, seed=0)
-    if spec is not None:   # batch 0's lengths
-        spec = dict(spec, **{n: None if spec[n] is None else spec[n][:1] for n in ("seq_len_q", "seq_len_kv")})
-        flops = 14.0 * w.E * visible_pairs(sub, spec)
-    else:
-        flops = sub.flops("fwd") + sub.flops("bwd")
-    del q, k, v, dO, mask
-    return (qs, ks, vs, dOs, ms), sub, flops, spec
+    if "bwd" not in w.phases:
+        return 2.0 * w.S * (w.E + w.Ev) + G * w.L * (2.0 * (w.E + w.Ev) + 4.0)
+    if spec is None:
+        one = w.with_(B=1, Hq=G, Hkv=1)
+        return one.flops("fwd") + one.flops("bwd")
+    sb = dict(spec, **{n: None if spec[n] is None else spec[n][b:b + 1] for n in ("seq_len_q", "seq_len_kv")})
+    return 14.0 * w.E * visible_pairs(w.with_(B=1, Hq=G, Hkv=1), sb)
 
 
-def cpu_oracle_sample(w, seconds_target=15.0, steps=None):
+def cpu_oracle_groups(w, seconds_target=12.0):
+    """The float64 oracle, as it stands, on whole KV groups of workload w in order (batch-major),
+    on the host cores: as many groups as fit in about `seconds_target` seconds, at least one.
+    Each KV group is a closed sub-problem (its query heads with all their queries and keys), so
+    the whole configuration's time is the sampled time scaled by the work of all groups over
+    that of the sampled ones ("extrapolated" unless every group ran)."""
     import oracle
-    (qs, ks, vs, dOs, ms), sub, flops, spec = _oracle_head_sample(w)
+    import workloads
+    fwd_only = "bwd" not in w.phases
+    q, k, v, dO, mask = workloads.make_inputs(w, seed=0, with_grad=not fwd_only)
+    spec = workloads.make_band(w, seed=0)
     band = None if spec is None else oracle.Band(spec["seq_len_q"], spec["seq_len_kv"], spec["alignment"],
                                                  spec["right_bound"], spec["left_bound"])
-    drop = oracle.Dropout(w.dropout, 0, 0) if w.dropout > 0 else None   # batch 0, head 0: the same mask rows
-    times = []
-    n = 0
-    t_start = time.perf_counter()
-    while True:
+    drop = oracle.Dropout(w.dropout, 0, 0) if w.dropout > 0 else None
+    groups = [(b, kv) for b in range(w.B) for kv in range(w.Hkv)]
+    done, t_sum, work = 0, 0.0, 0.0
+    for b, kv in groups:
         t0 = time.perf_counter()
-        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band, dropout=drop)
-        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, sub.Hq != sub.Hkv, band=band, dropout=drop)
-        times.append(time.perf_counter() - t0)
-        n += 1
-        if steps is not None and n >= steps:
+        oracle.ref_group(q, k, v, None if fwd_only else dO, b, kv, mask, w.scale, w.is_causal, band=band,
+                         dropout=drop)
+        t_sum += time.perf_counter() - t0
+        work += group_work(w, spec, b)
+        done += 1
+        if t_sum >= seconds_target:
             break
-        if steps is None and time.perf_counter() - t_start >= seconds_target:
-            break
-    t = statistics.median(times)
-    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{w.name}: batch 0, query head 0 (1 of {w.B * w.Hq} heads), forward+backward, "
-                      f"float64 NumPy, median of {n} runs of {t:.2f} s; BLAS default threads",
-            "seconds_per_sample": round(t, 3)}
+    total = sum(group_work(w, spec, b) for b, _ in groups)
+    unit, scale = ("GB/s", 1e9) if fwd_only else ("TFLOP/s", 1e12)
+    what = "forward" if fwd_only else "forward + backward"
+    return {"value": round(work / t_sum / scale, 6), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{w.name}: {done} of {len(groups)} KV groups (b, kv) in batch-major order, each "
+                      f"{w.Hq // w.Hkv} query heads with all their queries and keys, {what}, float64 NumPy "
+                      f"oracle, BLAS default threads; {t_sum:.2f} s",
+            "groups_timed": done, "groups_total": len(groups), "seconds_sampled": round(t_sum, 3),
+            "config_seconds": round(t_sum * total / work, 2), "extrapolated": done < len(groups)}
 
 
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
     import oracle
-    w = __import__("workloads").get(MAIN)
-    (qs, ks, vs, dOs, ms), sub, flops, _ = _oracle_head_sample(w)
-    gqa = sub.Hq != sub.Hkv
+    import workloads
+    w = workloads.get(MAIN)
+    q, k, v, dO, _ = workloads.make_inputs(w, seed=0)
+    # one query head (b = 0, h = 0) with all its queries and keys, forward + backward: a
+    # sample that keeps the run short even where the launcher gives BLAS one thread per rank
+    qs, ks, vs, dOs = q[:1, :1], k[:1, :1], v[:1, :1], dO[:1, :1]
+    del q, k, v, dO
+    flops = w.with_(B=1, Hq=1, Hkv=1).flops("fwd") + w.with_(B=1, Hq=1, Hkv=1).flops("bwd")
 
     def step():
-        oracle.ref_forward(qs, ks, vs, ms, w.scale, w.is_causal, gqa)
-        oracle.ref_backward(qs, ks, vs, dOs, ms, w.scale, w.is_causal, gqa)
+        oracle.ref_forward(qs, ks, vs, None, w.scale, w.is_causal)
+        oracle.ref_backward(qs, ks, vs, dOs, None, w.scale, w.is_causal)
 
     for _ in range(args.warmup):
         step()
@@ -655,8 +756,8 @@ def run_reference(args, ws, rank):
         step()
     t = (time.perf_counter() - t0) / args.steps
     value = flops / t / 1e12
-    sample = (f"{MAIN}: batch 0, query head 0 (1 of {w.B * w.Hq} heads) per step, forward+backward, "
-              f"float64 NumPy oracle; BLAS default threads")
+    sample = (f"{MAIN}: one query head (b=0, h=0: 1 of {w.B * w.Hq}, all its queries and keys) per step, "
+              f"forward + backward, float64 NumPy oracle; BLAS default threads")
     return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",

@@ -176,7 +176,9 @@ int sdpa_decode_num_splits(const sdpa_shape* shape);
  *
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Every call uses the same array and leaves its partials
+ * stream capture.  The address is kept per device and context: after the
+ * device's context is replaced (cudaDeviceReset), the next call looks it up
+ * again, and that call too should come before any capture.  Every call uses the same array and leaves its partials
  * there; each call overwrites all of the scratch it reads, so nothing needs
  * clearing between calls.  Calls whose work overlaps on the GPU (other streams,
  * other host threads) race on the array and corrupt each other's results:
@@ -314,9 +316,13 @@ sdpa_status sdpa_selftest_wait_timeout(void* stream /* cudaStream_t */);
 
 /* Reads and clears the current device's status word that kernels set when a
  * bounded device-side wait gives up.  Returns SDPA_OK when no kernel has timed
- * out since the last call.  Synchronises the device first (call it off the
- * hot path, e.g. in tests or after an error). */
-sdpa_status sdpa_last_device_status(void);
+ * out since the last call.  The read is enqueued on `stream` (a cudaStream_t;
+ * NULL is the default stream) after the work already there, and only that
+ * stream is synchronised: pass the stream the library's calls ran on.  Calls
+ * still running on other streams are not waited for, so their timeouts show
+ * on a later read.  A host-blocking call: keep it off the hot path (tests,
+ * after an error). */
+sdpa_status sdpa_last_device_status(void* stream /* cudaStream_t */);
 
 #ifdef __cplusplus
 }

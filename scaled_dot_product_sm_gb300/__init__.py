@@ -17,7 +17,6 @@ from __future__ import annotations
 
 import contextlib
 import ctypes
-import math
 import os
 from typing import Optional
 
@@ -157,7 +156,7 @@ def load_library(path: Optional[str] = None):
     lib.sdpa_decode_num_splits.restype = ctypes.c_int
     lib.sdpa_status_string.argtypes = [ctypes.c_int]
     lib.sdpa_status_string.restype = ctypes.c_char_p
-    lib.sdpa_last_device_status.argtypes = []
+    lib.sdpa_last_device_status.argtypes = [ctypes.c_void_p]
     lib.sdpa_last_device_status.restype = ctypes.c_int
     lib.sdpa_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
     lib.sdpa_selftest_wait_timeout.restype = ctypes.c_int
@@ -468,9 +467,10 @@ def sdpa_decode_paged(q, k_container, v_container, page_table_k, page_table_v, S
     return out, lse
 
 
-def last_device_status() -> int:
-    """Reads and clears the device status word (synchronises the device)."""
-    return int(load_library().sdpa_last_device_status())
+def last_device_status(stream=None) -> int:
+    """Reads and clears the device status word after the work on `stream` (default: torch's
+    current stream), synchronising that stream only."""
+    return int(load_library().sdpa_last_device_status(_stream(stream)))
 
 
 def selftest_wait_timeout(stream=None) -> None:
@@ -478,6 +478,3 @@ def selftest_wait_timeout(stream=None) -> None:
     up after about a second and records a timeout); read last_device_status() afterwards."""
     _raise(load_library().sdpa_selftest_wait_timeout(_stream(stream)), "sdpa_selftest_wait_timeout")
 
-
-def default_scale(E: int) -> float:
-    return 1.0 / math.sqrt(E)

@@ -24,6 +24,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned* g_status_ptr[kMaxDevices] = {};
+unsigned long long g_status_ctx[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_tried = false;
@@ -34,14 +35,46 @@ int current_device() {
   return d;
 }
 
+// cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points (no libcuda link).
+std::once_flag g_ctx_fn_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+}  // namespace
+
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_fn_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx || g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+namespace {
+
 unsigned* status_ptr() {
   const int d = current_device();
   if (d < 0) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[d]) {
+  // cudaGetSymbolAddress makes the runtime's context current if none is, so
+  // the id is read after it on a first lookup
+  const unsigned long long ctx = current_context_id();
+  if (!g_status_ptr[d] || ctx == 0 || ctx != g_status_ctx[d]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
     g_status_ptr[d] = static_cast<unsigned*>(ptr);
+    g_status_ctx[d] = current_context_id();
   }
   return g_status_ptr[d];
 }
@@ -619,13 +652,19 @@ sdpa_status sdpa_selftest_wait_timeout(void* stream) {
   return from_cuda(cudaGetLastError());
 }
 
-sdpa_status sdpa_last_device_status(void) {
-  if (cudaDeviceSynchronize() != cudaSuccess) return SDPA_ERR_CUDA;
+sdpa_status sdpa_last_device_status(void* stream) {
+  // Ordered after the work already on `stream` and synchronising only that
+  // stream: no other stream or host thread of the device waits for it.
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* word = status_ptr();
+  if (!word) return SDPA_ERR_CUDA;
   unsigned v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return SDPA_ERR_CUDA;
   if (v != 0) {
-    const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return SDPA_ERR_CUDA;
+    if (cudaMemsetAsync(word, 0, sizeof(v), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+      return SDPA_ERR_CUDA;
     return static_cast<sdpa_status>(v & 0xffu);
   }
   return SDPA_OK;

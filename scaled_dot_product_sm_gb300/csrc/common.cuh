@@ -212,8 +212,14 @@ bool decode_supported(int E, int Ev);
 int decode_rows_per_cta();
 int decode_stage_keys();
 // Device address and size of the fixed decode scratch on the current device
-// (looked up on first use per device).
+// (looked up on first use per device, and again when the device's context has
+// been replaced, e.g. after cudaDeviceReset).
 cudaError_t decode_static_scratch(void** ptr, size_t* bytes);
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context, 0 if no
+// context is current.  A device symbol's address belongs to one context: after
+// cudaDeviceReset the next context loads the module again, possibly elsewhere,
+// so cached symbol addresses are keyed on this id.
+unsigned long long current_context_id();
 
 // Tensor-map encoder obtained from the driver at run time (no libcuda link).
 bool encode_tmap_bf16_3d(void* tmap /* CUtensorMap* */, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,

@@ -457,6 +457,7 @@ namespace {
 constexpr int kScratchDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kScratchDevices] = {};
+unsigned long long g_scratch_ctx[kScratchDevices] = {};   // context the address belongs to
 }  // namespace
 
 cudaError_t decode_static_scratch(void** ptr, size_t* bytes) {
@@ -465,11 +466,15 @@ cudaError_t decode_static_scratch(void** ptr, size_t* bytes) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  // A cached address is reused only inside the context it was looked up in:
+  // after cudaDeviceReset the device's next context loads the array anew.
+  const unsigned long long ctx = current_context_id();
+  if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* addr = nullptr;
     e = cudaGetSymbolAddress(&addr, g_decode_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = addr;
+    g_scratch_ctx[dev] = current_context_id();
   }
   *ptr = g_scratch_addr[dev];
   *bytes = sizeof(g_decode_scratch);

@@ -53,3 +53,45 @@ def test_traffic_figures_are_dropped_when_the_source_differs():
     sha = bench.source_sha("fwd_tc_kernel.cuh", "ptx.cuh", "common.cuh")
     assert len(sha) == 16 and sha == bench.source_sha("fwd_tc_kernel.cuh", "ptx.cuh", "common.cuh")
     assert os.path.exists(os.path.join(bench.ROOT, "profiles", "traffic.json"))
+
+
+@pytest.mark.parametrize("name", ["gqa_causal_e128", "mha_causal_e64", "padded_seqlen_e128", "gqa_swa_e128",
+                                  "gqa_decode_s32k"])
+def test_group_work_sums_to_the_workload_total(name):
+    """The CPU baseline scales its sampled KV groups by work: the groups' work must add up to
+    the workload's (nominal FLOPs, visible-pair FLOPs, or the decode's bytes)."""
+    w = workloads.get(name)
+    spec = workloads.make_band(w, seed=0)
+    total = sum(bench.group_work(w, spec, b) for b in range(w.B) for _ in range(w.Hkv))
+    if "bwd" not in w.phases:
+        want = w.B * w.Hkv * w.S * (w.E + w.Ev) * 2 + w.B * w.Hq * w.L * ((w.E + w.Ev) * 2 + 4)
+    elif spec is None:
+        want = w.flops("fwd") + w.flops("bwd")
+    else:
+        want = 14.0 * w.E * bench.visible_pairs(w, spec)
+    assert total == pytest.approx(want, rel=1e-12)
+
+
+def test_computed_peak_is_sms_times_rate_times_clock():
+    assert bench.computed_peak_tflops(152, 2070.0) == pytest.approx(152 * 8182 * 2.07e9 / 1e12)
+
+
+def test_clock_sampler_keeps_only_the_samples_inside_its_window(tmp_path):
+    """Clock figures come from the samples taken between two host-time marks (the loops under
+    load), not from the idle samples around them."""
+    import datetime
+    t0 = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    path = tmp_path / "clocks.csv"
+    rows = []
+    for i, (mhz, cap) in enumerate([(1000, "Not Active"), (2070, "Not Active"), (2040, "Active"),
+                                    (2070, "Not Active"), (900, "Not Active")]):
+        ts = (t0 + datetime.timedelta(milliseconds=200 * i)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        rows.append(f"{ts}, 0, {mhz}, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, {cap}")
+    path.write_text("\n".join(rows) + "\n")
+    clk = bench.ClockSampler(0)
+    clk.proc, clk.path = object(), str(path)
+    clk.marks = {"a": t0 + datetime.timedelta(milliseconds=100), "b": t0 + datetime.timedelta(milliseconds=700)}
+    s = clk.summary("a", "b")
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070 and s["sm_mhz_min"] == 2040
+    assert s["reasons"] == ["sw_power_cap"]
+    assert clk.summary()["samples"] == 5

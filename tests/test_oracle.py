@@ -483,6 +483,23 @@ def test_group_and_rows_helpers_match_full():
         np.testing.assert_allclose(dVg, dVd[b, kv], atol=1e-13)
     # and the dropout is live there: without it the group's O differs
     assert np.abs(oracle.ref_group(q, k, v, None, 1, 1, mask, 0.5, False, band=band)[0] - Od[1, 2:4]).max() > 1e-3
+    # the row restriction's band and dropout branches: each row keeps its batch's lengths
+    # and its own (b, h, row) dropout counters
+    Ob, Lb = oracle.ref_forward(q, k, v, mask, 0.5, False, True, band=band)
+    for b, h, rows in ((0, 1, [1, 2, 5]), (1, 3, [0, 3, 4])):
+        Orb, Lrb = oracle.ref_forward_rows(q, k, v, b, h, rows, mask, 0.5, False, True, band=band)
+        np.testing.assert_allclose(Orb, Ob[b, h, rows], atol=1e-13)
+        np.testing.assert_array_equal(np.isneginf(Lrb), np.isneginf(Lb[b, h, rows]))
+        fin = np.isfinite(Lrb)
+        np.testing.assert_allclose(Lrb[fin], Lb[b, h, rows][fin], atol=1e-13)
+        Ord, Lrd = oracle.ref_forward_rows(q, k, v, b, h, rows, mask, 0.5, False, True, band=band, dropout=drop)
+        np.testing.assert_allclose(Ord, Od[b, h, rows], atol=1e-13)
+        np.testing.assert_allclose(Lrd[fin], Ld[b, h, rows][fin], atol=1e-13)
+    # both branches are live on these rows: dropping either changes the result
+    Orx, _ = oracle.ref_forward_rows(q, k, v, 1, 3, [0, 3, 4], mask, 0.5, False, True, band=band)
+    assert np.abs(Orx - Od[1, 3, [0, 3, 4]]).max() > 1e-3
+    Orx, _ = oracle.ref_forward_rows(q, k, v, 1, 3, [0, 3, 4], mask, 0.5, False, True)
+    assert np.abs(Orx - Ob[1, 3, [0, 3, 4]]).max() > 1e-3
 
 
 def test_repeated_keys_equal_log_multiplicity_bias():

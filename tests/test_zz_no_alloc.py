@@ -5,9 +5,12 @@ inside another runtime that gets no scratch space, or a serving loop whose
 device memory is fixed at start-up and may not call cudaMalloc afterwards.
 sdpa_decode_noalloc gives them the split-KV decode with its split partials in
 the library's own fixed device array instead of a caller workspace.  These
-checks call it through the C ABI and compare it with sdpa_decode (which takes
-a workspace), call after call: the shared array keeps the previous call's
-partials, so a second call with other inputs must not see stale data.
+checks call it through the C ABI, call after call, and compare each result
+with the float64 oracle (the tolerances of every bf16 parity test) and with
+sdpa_decode (which takes a workspace) at the same split count: both run the
+same kernels on the same partial layout, so the two must agree bit for bit.
+The shared array keeps the previous call's partials, so a second call with
+other inputs must not see stale data.
 
 This file is named to be collected last.
 """
@@ -17,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import scaled_dot_product_sm_gb300 as sdpa
 from workloads import random_inputs
 
@@ -48,17 +52,25 @@ def _noalloc(lib, q, k, v, mask, scale, gqa, splits):
     return st, o, lse
 
 
-def _compare(o, lse, o_ref, lse_ref):
+def _against_oracle(o, lse, q, k, v, mask):
+    """o, lse of a decode call against the float64 oracle on the same (CPU) inputs."""
+    ref_o, ref_lse = oracle.ref_forward(q.cpu(), k.cpu(), v.cpu(), None if mask is None else mask.cpu(), None,
+                                        False, True)
     a = o.float().cpu().double().numpy()
-    r = o_ref.float().cpu().double().numpy()
     assert np.isfinite(a).all()
-    rel = np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30)
+    rel = np.linalg.norm(a - ref_o) / max(np.linalg.norm(ref_o), 1e-30)
     assert rel <= O_REL_L2, rel
-    la, lr = lse.cpu().double().numpy(), lse_ref.cpu().double().numpy()
-    assert np.array_equal(np.isneginf(la), np.isneginf(lr))
-    fin = np.isfinite(lr)
-    assert fin.any()
-    assert np.abs(la[fin] - lr[fin]).max() <= LSE_ABS
+    la = lse.cpu().double().numpy()
+    dead = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(la), dead)
+    assert np.all(a[dead] == 0.0)
+    assert (~dead).any()
+    assert np.abs(la[~dead] - ref_lse[~dead]).max() <= LSE_ABS
+
+
+def _bit_identical(o, lse, o_ref, lse_ref):
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
 
 
 CALLS = [
@@ -68,18 +80,19 @@ CALLS = [
 ]
 
 
-def test_noalloc_matches_workspace_decode_on_consecutive_calls(lib):
+def test_noalloc_matches_oracle_and_workspace_decode_on_consecutive_calls(lib):
     for B, Hq, Hkv, L, S, E, with_mask, splits, seed in CALLS:
         q, k, v, _, mask = random_inputs(B, Hq, Hkv, L, S, E, E, torch.bfloat16, seed=seed,
                                          mask_kind="bias" if with_mask else "none", mask_shape=(1, Hq),
                                          full_rows=1 if with_mask else 0)
-        q, k, v = q.cuda(), k.cuda(), v.cuda()
-        mask = None if mask is None else mask.cuda()
-        o_ref, lse_ref = sdpa.sdpa_decode(q, k, v, mask, None, True, splits)
-        st, o, lse = _noalloc(lib, q, k, v, mask, None, True, splits)
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        md = None if mask is None else mask.cuda()
+        st, o, lse = _noalloc(lib, qd, kd, vd, md, None, True, splits)
+        o_ref, lse_ref = sdpa.sdpa_decode(qd, kd, vd, md, None, True, splits)
         torch.cuda.synchronize()
         assert st == 0, lib.sdpa_status_string(st)
-        _compare(o, lse, o_ref, lse_ref)
+        _against_oracle(o, lse, q, k, v, mask)
+        _bit_identical(o, lse, o_ref, lse_ref)
     assert sdpa.last_device_status() == 0
 
 
@@ -93,4 +106,5 @@ def test_noalloc_rejects_scratch_beyond_the_maximum(lib):
     o_ref, lse_ref = sdpa.sdpa_decode(q, k, v, None, None, True, 16)
     torch.cuda.synchronize()
     assert st == 0
-    _compare(o, lse, o_ref, lse_ref)
+    _against_oracle(o, lse, q, k, v, None)
+    _bit_identical(o, lse, o_ref, lse_ref)
