@@ -21,14 +21,17 @@
 //        P^T  = exp2(S^T alpha log2e + mask log2e - lse log2e),  dS^T = P^T o (dP^T - D)
 //        dV  += P^T dO,  dK += dS^T Q       (A operands P^T, dS^T read from TMEM)
 //        dQ^T = K^T dS^T                    (TMEM, 128 head dims x 64 queries; dS^T also in smem)
-//     dQ^T is staged in shared memory as dQ rows and added (without alpha) to
-//     the global fp32 accumulator with one TMA bulk reduction per tile (the
-//     reduction runs in L2, full lines, one instruction);
+//     dQ^T goes from TMEM to the drain warps' registers and is added (without
+//     alpha) to the global fp32 accumulator by reductions in L2: for each query
+//     a warp adds 32 consecutive floats, one full 128-byte line.  Nothing is
+//     staged in shared memory, whose bandwidth the SS MMAs (K and Q, V and dO,
+//     K^T and dS^T) already use heavily; the 32 KB saved give the masked
+//     variant its third query-tile stage;
 //  3. dQ = bf16(alpha * accumulator).
 // Warp roles (512 threads, four warpgroups with a register split):
 //   warps 0-7   elementwise (thread = key = TMEM lane; warps w and w+4 share
 //               the lane quarter and take query columns 0-31 / 32-63)    152 regs
-//   warps 8-11  dQ drain and staging (thread = head dim = TMEM lane)     136 regs
+//   warps 8-11  dQ drain (thread = head dim = TMEM lane)                  136 regs
 //   warp  12    TMA producer                                              72 regs
 //   warp  13    TMEM allocator and issuer of the gradient MMAs (dV, dK, dQ^T)
 //   warp  14    issuer of the score MMAs (S^T, dP^T)
@@ -76,8 +79,8 @@ template <int E_, bool MSTAGE>
 struct BwdCfg {
   static constexpr int E = E_, Ev = E_;
   static constexpr int ECH = E / 64;                          // 64-element column blocks
-  // query-tile stages (prefetch two tiles ahead; one when the mask tile takes the room at E = 128)
-  static constexpr int NSQ = (E == 128 && MSTAGE) ? 2 : 3;
+  // query-tile stages: prefetch two tiles ahead (with or without the staged mask tile)
+  static constexpr int NSQ = 3;
   static constexpr int kKBytes = ECH * BKV * 128;             // K tile: ECH blocks of [128 keys x 64 dims]
   static constexpr int kQTile = ECH * BQ * 128;               // Q (or dO) tile: ECH blocks of [64 rows x 64 dims]
   static constexpr int kStage = 2 * kQTile + 1024;            // Q, dO, rowstats (512 B, padded)
@@ -86,8 +89,7 @@ struct BwdCfg {
   static constexpr int kOffV = kOffK + kKBytes;
   static constexpr int kOffStage = kOffV + kKBytes;
   static constexpr int kOffDS = kOffStage + NSQ * kStage;     // dS^T [128 keys x 64 queries] bf16
-  static constexpr int kOffDQ = kOffDS + BKV * 128;           // dQ staging [64 queries x E] fp32
-  static constexpr int kOffMask = kOffDQ + BQ * E * 4;        // mask tile (TMA, one iteration ahead)
+  static constexpr int kOffMask = kOffDS + BKV * 128;         // mask tile (TMA, one iteration ahead)
   static constexpr int kOffBar = kOffMask + kMaskBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static_assert(E == 64 || E == 128, "head width");
@@ -102,17 +104,9 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void named_bar(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+__device__ __forceinline__ void red_add_f32(float* gdst, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gdst), "f"(v) : "memory");
 }
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 struct TcBwdArgs {
   BwdParams p;
@@ -185,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int E = C::E, Ev = C::Ev, ECH = C::ECH;
   constexpr int kKBytes = C::kKBytes, kQTile = C::kQTile, kStage = C::kStage;
   constexpr int kOffK = C::kOffK, kOffV = C::kOffV, kOffStage = C::kOffStage, kOffDS = C::kOffDS,
-                kOffDQ = C::kOffDQ, kOffBar = C::kOffBar;
+                kOffBar = C::kOffBar;
   const BwdParams& p = a.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -598,7 +592,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ dQ drain (thread = head dim)
     const int e = (warp - 8) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 8) * 32) << 16;
-    float* stage_dq = reinterpret_cast<float*>(smem + kOffDQ);
     TileIter ti = tile0;
     for (int i = 0; i < n; ++i, ti.next()) {
       const int qt = ti.qt, g = ti.g;
@@ -612,25 +605,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free);
-      // the previous bulk reduction must have finished reading the staging rows
-      if (e == 0) bulk_wait_read_all();
-      named_bar(1, 128);
-      if (e < E) {   // dQ^T lanes past E are padding of the M = 128 MMA
-#pragma unroll
-        for (int j = 0; j < 32; ++j) stage_dq[j * E + e] = __uint_as_float(v0[j]);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) stage_dq[(32 + j) * E + e] = __uint_as_float(v1[j]);
-      }
-      fence_proxy_async_smem();
-      named_bar(1, 128);
-      if (e == 0) {
+      // dQ rows straight from registers: for each query, the 32 lanes of a warp add 32
+      // consecutive floats (one 128-byte line) of the fp32 accumulator in L2
+      if (e < E) {
+        float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.L + q0) * E + e;
         const int nq = min(BQ, p.L - q0);
-        bulk_reduce_add_f32(p.dq_acc + (static_cast<size_t>(bh) * p.L + q0) * E, stage_dq,
-                            static_cast<uint32_t>(nq) * E * 4);
-        bulk_commit();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nq) red_add_f32(dst + static_cast<size_t>(j) * E, __uint_as_float(v0[j]));
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 + j < nq) red_add_f32(dst + static_cast<size_t>(32 + j) * E, __uint_as_float(v1[j]));
       }
     }
-    if (e == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
