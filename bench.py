@@ -66,8 +66,9 @@ def parse():
                     choices=["tiny_f32", "tiny_f32_causal", "mha_causal_e64", "gqa_causal_e128", "padded_mask_e128",
                              "padded_seqlen_e128", "gqa_swa_e128", "gqa_causal_dropout_e128"],
                     help="prefill workload of the step (default: the GQA causal E=128 headline workload)")
-    ap.add_argument("--phase", choices=["all", "fwd", "bwd", "decode"], default="all",
-                    help="profiling aid: run only the forward loop, the backward loop or the decode leg")
+    ap.add_argument("--phase", choices=["all", "fwd", "bwd", "decode", "paged"], default="all",
+                    help="profiling aid: run only the forward loop, the backward loop, or the dense or paged "
+                         "decode leg")
     ap.add_argument("--summarize-launches", metavar="CSV",
                     help="print a per-kernel summary of an ncu launch list (gpu__time_duration.sum, --csv) and exit")
     args = ap.parse_args()
@@ -309,8 +310,8 @@ def run_ours(args, ws, rank, local):
         sdpa.sdpa_backward(q, k, v, o, dO, lse, mask, scale, w.is_causal, w.enable_gqa, dq=dq, dk=dk, dv=dv,
                            workspace=bws, band=band, dropout=drop)
 
-    if args.phase == "decode":
-        return run_decode_only(args, ws, local, dev, peaks)
+    if args.phase in ("decode", "paged"):
+        return run_decode_only(args, ws, local, dev, peaks, paged=args.phase == "paged")
     fwd_only = args.phase == "fwd"
     if args.phase == "bwd":
         fwd()
@@ -597,13 +598,8 @@ def run_ours(args, ws, rank, local):
         nbs = wd.S // bsz
         perm = torch.randperm(wd.B * nbs, generator=torch.Generator().manual_seed(1)).to(dev)
 
-        def to_container(x):
-            blocks = x.reshape(wd.B, wd.Hkv, nbs, bsz, x.shape[3]).permute(0, 2, 1, 3, 4).reshape(
-                wd.B * nbs, wd.Hkv, bsz, x.shape[3])
-            c = torch.empty_like(blocks)
-            c[perm] = blocks
-            return c
-        kc, vc = to_container(kd), to_container(vd)
+        kc = paged_container(kd, wd.B, wd.Hkv, wd.S, bsz, perm)
+        vc = paged_container(vd, wd.B, wd.Hkv, wd.S, bsz, perm)
         del kd, vd
         table = perm.reshape(wd.B, nbs).to(torch.int32).contiguous()
 
@@ -664,7 +660,18 @@ def run_ours(args, ws, rank, local):
     return line
 
 
-def run_decode_only(args, ws, local, dev, peaks):
+def paged_container(x, B, Hkv, S, bsz, perm):
+    """Dense cache [B, Hkv, S, D] as a paged container: its bsz-key blocks in the shuffled order
+    `perm` (block b * (S / bsz) + i of the cache goes to container block perm[...])."""
+    import torch
+    nbs = S // bsz
+    blocks = x.reshape(B, Hkv, nbs, bsz, x.shape[3]).permute(0, 2, 1, 3, 4).reshape(B * nbs, Hkv, bsz, x.shape[3])
+    c = torch.empty_like(blocks)
+    c[perm] = blocks
+    return c
+
+
+def run_decode_only(args, ws, local, dev, peaks, paged=False):
     import torch
 
     import scaled_dot_product_sm_gb300 as sdpa
@@ -675,10 +682,21 @@ def run_decode_only(args, ws, local, dev, peaks):
     od = torch.empty(wd.B, wd.Hq, 1, wd.Ev, dtype=qd.dtype, device=dev)
     lsed = torch.empty(wd.B, wd.Hq, 1, dtype=torch.float32, device=dev)
     dws = torch.empty(max(16, sdpa.decode_workspace_bytes(qd, kd, vd, 0)), dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup + args.steps):
-        sdpa.sdpa_decode(qd, kd, vd, None, wd.scale, True, 0, out=od, lse=lsed, workspace=dws)
+    if paged:   # 64-key blocks of every sequence shuffled in one container, as in the bench's paged leg
+        bsz = 64
+        perm = torch.randperm(wd.B * (wd.S // bsz), generator=torch.Generator().manual_seed(1)).to(dev)
+        kc = paged_container(kd, wd.B, wd.Hkv, wd.S, bsz, perm)
+        vc = paged_container(vd, wd.B, wd.Hkv, wd.S, bsz, perm)
+        del kd, vd
+        table = perm.reshape(wd.B, wd.S // bsz).to(torch.int32).contiguous()
+        for _ in range(args.warmup + args.steps):
+            sdpa.sdpa_decode_paged(qd, kc, vc, table, table, wd.S, None, wd.scale, True, 0, out=od, lse=lsed,
+                                   workspace=dws)
+    else:
+        for _ in range(args.warmup + args.steps):
+            sdpa.sdpa_decode(qd, kd, vd, None, wd.scale, True, 0, out=od, lse=lsed, workspace=dws)
     torch.cuda.synchronize()
-    return {"phase": "decode", "status": sdpa.last_device_status()}
+    return {"phase": "paged" if paged else "decode", "status": sdpa.last_device_status()}
 
 
 # ------------------------------------------------------------------ CPU oracle

@@ -28,6 +28,9 @@
 //     K^T and dS^T) already use heavily; the 32 KB saved give the masked
 //     variant its third query-tile stage;
 //  3. dQ = bf16(alpha * accumulator).
+// The main kernel and the conversion are programmatic dependent launches: each
+// starts while the grid before it finishes, and waits for it (griddepcontrol)
+// before touching its results, which hides their launch and set-up.
 // Warp roles (512 threads, four warpgroups with a register split):
 //   warps 0-7   elementwise (thread = key = TMEM lane; warps w and w+4 share
 //               the lane quarter and take query columns 0-31 / 32-63)    152 regs
@@ -117,6 +120,8 @@ struct TcBwdArgs {
 
 template <int E>
 __global__ void __launch_bounds__(256) bwd_rowstats_kernel(TcBwdArgs a) {
+  // the main kernel may launch as soon as every block of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const BwdParams& p = a.p;
   const long long rows = static_cast<long long>(p.B) * p.Hq * a.Lpad;
   const long long gr = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -154,6 +159,7 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(TcBwdArgs a) {
 
 template <int E>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the main kernel's accumulator is complete
   const float sc = p.scale;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
@@ -266,6 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched behind the row statistics (programmatic dependent launch), so this
+  // set-up overlaps their tail: every role reads what that grid writes, so all
+  // wait for it here; then the conversion grid may launch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp >= 12) {
     regs_dec<kRegsOther>();
@@ -664,12 +675,28 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
     return e;
   const unsigned groups = static_cast<unsigned>(p.B * p.Hkv), ktiles = static_cast<unsigned>((p.S + BKV - 1) / BKV);
   const dim3 grid = p.band.right >= 0 ? dim3(groups, ktiles) : dim3(ktiles, groups);
-  kern<<<grid, kThreads, C::kSmemBytes, st>>>(tmK, tmV, tmQ, tmdO, tmM, a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // programmatic dependent launches: each grid may start while the previous one
+  // finishes and waits for it (griddepcontrol.wait) before reading its results
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, tmQ, tmdO, tmM, a)) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;
   const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n8 + 255) / 256, 152 * 16));
-  bwd_dq_convert_kernel<E><<<blocks, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg2 = {};
+  cfg2.gridDim = dim3(blocks);
+  cfg2.blockDim = dim3(256);
+  cfg2.stream = st;
+  cfg2.attrs = &attr;
+  cfg2.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg2, bwd_dq_convert_kernel<E>, p);
 }
 
 template <bool DROP, bool MSTAGE>
