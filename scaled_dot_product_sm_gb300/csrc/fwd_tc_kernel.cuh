@@ -102,9 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = empty + NS;         // 2: S_t(j) (and PV_t(j-1)) complete
   uint64_t* p_full = s_full + 2;         // 2: P_t(j) in TMEM (one arrival per warp)
   uint64_t* o_final = p_full + 2;        // 2: the last PV_t of the unit complete
-  uint64_t* mk_full = o_final + 2;       // 2: staged mask tile of query tile t landed
-  uint64_t* mk_empty = mk_full + 2;      // 2: ... and read by tile t's softmax warps
-  uint64_t* un_full = mk_empty + 2;      // 4: unit index published (taken from the counter)
+  uint64_t* mk_full = o_final + 2;       // 4: staged mask half h of query tile t landed (2t + h)
+  uint64_t* mk_empty = mk_full + 4;      // 4: ... and read by tile t's softmax warps
+  uint64_t* un_full = mk_empty + 4;      // 4: unit index published (taken from the counter)
   uint64_t* un_empty = un_full + 4;      // 4: ... and read by every role
   int* un_slot = reinterpret_cast<int*>(un_empty + 4);                  // 4 unit indices
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(un_slot + 4);
@@ -192,8 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);
       mbar_init(&o_final[t], 1);
-      mbar_init(&mk_full[t], 1);
-      mbar_init(&mk_empty[t], 4);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&mk_full[2 * t + h], 1);
+        mbar_init(&mk_empty[2 * t + h], 4);
+      }
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&un_full[i], 1);
@@ -343,13 +345,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (MK == kMaskStaged && warp == 10 && lane == 0) {
     // ------------------------------------------------------------ mask producer
-      // One buffer, filled in the softmax warps' order of use: key tile j of query
-      // tile 0, then of tile 1, then j + 1 ...  Each tile has its own full/empty
-      // pair, so a wait never has to tell apart two phases of the same parity;
-      // a fill waits until the previous fill (of either tile) has been read.
+      // One buffer in two halves (keys 0-63 and 64-127 of a key tile), filled in the
+      // softmax warps' order of use: key tile j of query tile 0, then of tile 1, then
+      // j + 1 ...  Each (tile, half) has its own full/empty pair, so a wait never has
+      // to tell apart two phases of the same parity; a half is refilled as soon as
+      // the previous fill of that half (of either tile) has been read, so the next
+      // tile's first half is in flight while the softmax still waits for the second.
       prefetch_tmap(&tmM);
       const long long LS = static_cast<long long>(p.L) * p.S;
-      int cnt[2] = {0, 0}, last = -1;
+      int cnt[2] = {0, 0}, last[2] = {-1, -1};   // fills per tile; tile that last filled half h
       for (int ur = 0;; ++ur) {
         const int k = read_unit(ur);
         if (dyn) mbar_arrive(&un_empty[ur & 3]);
@@ -361,23 +365,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 2; ++t) {
             const int row_first = u.r0 + t * BM;
             if (row_first >= p.L || j < u.a[t] || j >= u.e[t]) continue;
-            if (last >= 0)
-              mbar_wait(&mk_empty[last], (cnt[last] - 1) & 1, abort_flag, p.status, status_code(0x1b));
-            mbar_arrive_expect_tx(&mk_full[t], C::kMaskBytes);
 #pragma unroll
-            for (int q = 0; q < BN / 32; ++q)
-              tma_load_3d(smem + C::kOffMask + q * (BM * 128), &tmM, &mk_full[t], j * BN + 32 * q, row_first, slice);
+            for (int h = 0; h < 2; ++h) {
+              if (last[h] >= 0)
+                mbar_wait(&mk_empty[2 * last[h] + h], (cnt[last[h]] - 1) & 1, abort_flag, p.status, status_code(0x1b));
+              mbar_arrive_expect_tx(&mk_full[2 * t + h], C::kMaskBytes / 2);
+#pragma unroll
+              for (int q = 2 * h; q < 2 * h + 2; ++q)   // 32-key boxes of this half
+                tma_load_3d(smem + C::kOffMask + q * (BM * 128), &tmM, &mk_full[2 * t + h], j * BN + 32 * q, row_first,
+                            slice);
+              last[h] = t;
+            }
             if (j + 1 < u.e[t])   // the tile's next key tile into L2 now, so its fill is an L2 hit
 #pragma unroll
               for (int q = 0; q < BN / 32; ++q) tma_prefetch_l2_3d(&tmM, (j + 1) * BN + 32 * q, row_first, slice);
             ++cnt[t];
-            last = t;
           }
         }
       }
       if (*abort_flag)   // a wait gave up: let this thread's copies land before the CTA exits
         for (int t = 0; t < 2; ++t)
-          if (cnt[t] > 0) mbar_drain(&mk_full[t], static_cast<uint32_t>((cnt[t] - 1) & 1));
+          if (cnt[t] > 0)
+            for (int h = 0; h < 2; ++h) mbar_drain(&mk_full[2 * t + h], static_cast<uint32_t>((cnt[t] - 1) & 1));
     }
   } else {
     regs_inc<kRegsSoftmax>();
@@ -437,23 +446,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Rows past L (mrow == nullptr) read nothing.  Staged: the row from shared
           // memory (zero-filled past L and S), then the buffer goes back to the producer.
           if (MK == kMaskStaged) {
-            mbar_wait(&mk_full[t], mk_cnt & 1, abort_flag, p.status, status_code(0x1c));
-            ++mk_cnt;
             const uint8_t* ms = smem + C::kOffMask + r * 128;
 #pragma unroll
-            for (int q = 0; q < BN / 32; ++q)
+            for (int h = 0; h < 2; ++h) {   // keys 64h .. 64h + 63: two 32-key boxes
+              mbar_wait(&mk_full[2 * t + h], mk_cnt & 1, abort_flag, p.status, status_code(0x1c));
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const float4 mv = *reinterpret_cast<const float4*>(ms + q * (BM * 128) + ((c ^ (r & 7)) << 4));
-                x[32 * q + 4 * c + 0] = mv.x;
-                x[32 * q + 4 * c + 1] = mv.y;
-                x[32 * q + 4 * c + 2] = mv.z;
-                x[32 * q + 4 * c + 3] = mv.w;
-              }
-            // the next fill is a TMA (async-proxy) write: order this lane's reads before it
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&mk_empty[t]);
+              for (int q = 2 * h; q < 2 * h + 2; ++q)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const float4 mv = *reinterpret_cast<const float4*>(ms + q * (BM * 128) + ((c ^ (r & 7)) << 4));
+                  x[32 * q + 4 * c + 0] = mv.x;
+                  x[32 * q + 4 * c + 1] = mv.y;
+                  x[32 * q + 4 * c + 2] = mv.z;
+                  x[32 * q + 4 * c + 3] = mv.w;
+                }
+              // the next fill is a TMA (async-proxy) write: order this lane's reads before it
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&mk_empty[2 * t + h]);
+            }
+            ++mk_cnt;
           } else if (mask_v8) {
             const float* mtile = mrow + kb;
 #pragma unroll
