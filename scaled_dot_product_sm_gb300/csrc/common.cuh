@@ -82,8 +82,11 @@ __device__ __forceinline__ void philox4x32_10(unsigned c0, unsigned c1, unsigned
   constexpr unsigned kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const unsigned hi0 = __umulhi(c0, kM0), lo0 = c0 * kM0;
-    const unsigned hi1 = __umulhi(c2, kM1), lo1 = c2 * kM1;
+    // one 32 x 32 -> 64-bit multiply gives both halves of each product
+    const unsigned long long p0 = static_cast<unsigned long long>(c0) * kM0;
+    const unsigned long long p1 = static_cast<unsigned long long>(c2) * kM1;
+    const unsigned hi0 = static_cast<unsigned>(p0 >> 32), lo0 = static_cast<unsigned>(p0);
+    const unsigned hi1 = static_cast<unsigned>(p1 >> 32), lo1 = static_cast<unsigned>(p1);
     c0 = hi1 ^ c1 ^ k0;
     c1 = lo1;
     c2 = hi0 ^ c3 ^ k1;
