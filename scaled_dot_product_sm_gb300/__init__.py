@@ -248,9 +248,12 @@ def _band_tensors(band):
 
 
 def _on_device(t):
-    """Makes t's device current for the call, so the library launches there and on its stream."""
+    """Makes t's device current for the call, so the library launches there and on its stream
+    (no switch when it is current already)."""
     import torch
-    return torch.cuda.device(t.device) if t.is_cuda else contextlib.nullcontext()
+    if not t.is_cuda or t.device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(t.device)
 
 
 def _ptr(t):
@@ -319,9 +322,13 @@ def _forward(shp, q, k, v, mask, scale, is_causal, enable_gqa, out, lse, workspa
         out = torch.empty(B, Hq, L, v.shape[3], dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
-    need = int(lib.sdpa_forward_workspace_bytes(ctypes.byref(shp)))
-    if workspace is None and need:
-        workspace = _workspace(need, q.device)
+    # the workspace holds the decode route's split partials (one query row) or the unit
+    # counter of calls with padding lengths; other calls run without one
+    if workspace is None and (L == 1 or (band is not None and (band.seq_len_q is not None
+                                                             or band.seq_len_kv is not None))):
+        need = int(lib.sdpa_forward_workspace_bytes(ctypes.byref(shp)))
+        if need:
+            workspace = _workspace(need, q.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if band is None and dropout is not None:
         band = Band(right_bound=0 if is_causal else None)

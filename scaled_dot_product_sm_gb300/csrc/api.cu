@@ -62,6 +62,37 @@ unsigned long long current_context_id() {
 }
 
 namespace {
+std::mutex g_prep_mu;
+struct Prepared {
+  const void* kernel;
+  unsigned long long ctx;
+  int smem;
+};
+Prepared g_prepared[256];
+int g_nprepared = 0;
+}  // namespace
+
+cudaError_t prepare_kernel(const void* kernel, int smem_bytes, int regs) {
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lk(g_prep_mu);
+  if (ctx != 0)
+    for (int i = 0; i < g_nprepared; ++i)
+      if (g_prepared[i].kernel == kernel && g_prepared[i].ctx == ctx && g_prepared[i].smem == smem_bytes)
+        return cudaSuccess;
+  if (regs > 0) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != regs) return cudaErrorInvalidConfiguration;
+  }
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  const unsigned long long now = current_context_id();   // the calls above make a context current
+  if (now != 0 && g_nprepared < 256) g_prepared[g_nprepared++] = Prepared{kernel, now, smem_bytes};
+  return cudaSuccess;
+}
+
+namespace {
 
 unsigned* status_ptr() {
   const int d = current_device();

@@ -650,10 +650,8 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
   a.mslice_h = static_cast<int>(p.mask_sh / LS);
   auto kern = bwd_tc_kernel<E, DROP, MSTAGE>;
   // The register split in the main kernel assumes the launch reserves exactly kRegsLaunch per thread.
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, kRegsLaunch);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const long long srows = static_cast<long long>(p.B) * p.Hq * a.Lpad;
   bwd_rowstats_kernel<E><<<static_cast<unsigned>((srows + 7) / 8), 256, 0, st>>>(a);
   e = cudaGetLastError();
@@ -671,8 +669,6 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
     if (!encode_tmap_f32_3d(&tmM, p.mask, p.S, p.L, static_cast<uint64_t>(slices), BKV, BQ, false))
       return cudaErrorInvalidValue;
   }
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) != cudaSuccess)
-    return e;
   const unsigned groups = static_cast<unsigned>(p.B * p.Hkv), ktiles = static_cast<unsigned>((p.S + BKV - 1) / BKV);
   const dim3 grid = p.band.right >= 0 ? dim3(groups, ktiles) : dim3(ktiles, groups);
   // programmatic dependent launches: each grid may start while the previous one

@@ -223,6 +223,12 @@ cudaError_t decode_static_scratch(void** ptr, size_t* bytes);
 // cudaDeviceReset the next context loads the module again, possibly elsewhere,
 // so cached symbol addresses are keyed on this id.
 unsigned long long current_context_id();
+// Once per kernel and CUDA context: checks that the kernel is compiled for
+// `regs` registers per thread (0: no check; warp-specialised kernels split
+// exactly that many with setmaxnreg) and opts it in to `smem_bytes` of dynamic
+// shared memory.  cudaFuncGetAttributes and cudaFuncSetAttribute cost
+// microseconds of host time each; later launches in the same context skip them.
+cudaError_t prepare_kernel(const void* kernel, int smem_bytes, int regs);
 
 // Tensor-map encoder obtained from the driver at run time (no libcuda link).
 bool encode_tmap_bf16_3d(void* tmap /* CUtensorMap* */, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,

@@ -415,7 +415,7 @@ cudaError_t run(const DecodeParams& dp, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   auto kern = decode_split_kernel<ECH, VCH, NSTAGE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), SM::kBytes, 0);
   if (e != cudaSuccess) return e;
   const int nrg = (p.G * p.L + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid(dp.nsplit, p.B * p.Hkv * nrg);

@@ -655,16 +655,10 @@ cudaError_t run(const FwdParams& p, cudaStream_t st) {
   }
   auto kern = fwd_tc_kernel<ECH, VCH, MK, DROP>;
   // The register split in the kernel assumes the launch reserves exactly kRegsLaunch per thread.
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kBytes, kRegsLaunch);
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(p.B) * p.Hq * ((p.L + 2 * BM - 1) / (2 * BM));
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int sms = num_sms();
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);   // persistent: one CTA per SM
   kern<<<grid, kThreads, C::kBytes, st>>>(tmQ, tmK, tmV, tmM, p);
   return cudaGetLastError();
