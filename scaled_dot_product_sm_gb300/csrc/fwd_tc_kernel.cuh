@@ -14,7 +14,7 @@
 //   warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax of query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through a ring
-//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+//   warp  9    TMEM allocator and tcgen05.mma issuer (see below)
 //   warp  10   stages the additive mask by TMA (rows of a multiple of 4 keys), else idle
 //   warp  11   idle (it completes the third warpgroup)
 // The third warpgroup hands registers to the softmax warpgroups (72 -> 216 per
@@ -32,6 +32,15 @@
 // than 2^8 (the stale max keeps every p below 256, and O/l is exact either way).
 // Causal: key tiles entirely above the diagonal are neither loaded nor
 // computed; only tiles that cross it test j <= i per element.
+// The issuer paces the whole kernel: each tile's chain is its softmax, then
+// PV_t(j) and S_t(j+1) behind the other tile's MMAs, so every cycle the issuing
+// thread spends between MMA groups (barrier waits, commits, descriptor
+// arithmetic) lengthens it.  Without a staged mask the whole of warp 9 runs
+// the issue loop, converged, and the lane elect.sync picks issues each MMA and
+// commit: the operand arithmetic is then warp-uniform, and the causal E = 128
+// forward runs 7.5 % faster than with lane 0 alone in a divergent branch.  With
+// the staged mask, where the softmax rather than the issuer sets the pace, lane 0
+// alone measured 1 % faster, so that instantiation keeps it.
 #pragma once
 
 #include <cuda.h>
@@ -90,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM, FwdParams p) {
   constexpr bool MASKED = MK != kMaskNone;
+  constexpr bool kWarpIssue = MK != kMaskStaged;   // the MMA issuer: all of warp 9, or lane 0 alone
   using C = FwdCfg<ECH, VCH, MK>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -258,8 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nunits > 0) mbar_drain(bar_q, static_cast<uint32_t>((nunits - 1) & 1));
         mbar_drain_ring(full, NS, it);
       }
-    } else if (warp == 9 && lane == 0) {
+    } else if (warp == 9 && (kWarpIssue || lane == 0)) {
     // ------------------------------------------------------------ MMA issuer
+      // the one lane that issues (all of them, when lane 0 alone runs this loop)
+      auto leader = [&]() { return !kWarpIssue || elect_one(); };
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);        // Q (K-major) x K (K-major)
       constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (TMEM, K-major) x V (MN-major)
       // Operand descriptors, built once; a K-step, a tile or a ring slot moves only the start address.
@@ -271,26 +283,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < C::E / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          umma_ss(tmem + t * BN, qa + off, ka + off, idesc_s, kk > 0);
+          if (leader()) umma_ss(tmem + t * BN, qa + off, ka + off, idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
         const SmemDesc va = dv + slot * C::kItem;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 8 TMEM columns of bf16 pairs per step
-          umma_ts(tmem + 256 + t * 128, tmem + t * BN + kk * 8, va + kk * 16 * 128, idesc_o,
+          if (leader()) umma_ts(tmem + 256 + t * 128, tmem + t * BN + kk * 8, va + kk * 16 * 128, idesc_o,
                   (acc || kk > 0) ? 1u : 0u);
       };
       int it = 0;               // ring position, continued across units
       uint32_t pc[2] = {0, 0};  // p_full completions consumed per tile
       for (int r = 0;; ++r) {
         const int k = read_unit(r);
-        if (dyn) mbar_arrive(&un_empty[r & 3]);
+        if (dyn && lane == 0) mbar_arrive(&un_empty[r & 3]);
         if (k < 0) break;
         const Unit u = unit_at(k);
         mbar_wait(bar_q, r & 1, abort_flag, p.status, status_code(0x12));
         if (u.j1 == u.j0) {
-          umma_commit(q_free);   // nothing to compute; covers the earlier units' MMAs
+          if (leader()) umma_commit(q_free);   // nothing to compute; covers the earlier units' MMAs
           continue;
         }
         {
@@ -300,10 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 2; ++t) {
             if (u.a[t] != u.j0 || u.e[t] == u.a[t]) continue;
             issue_s(t, s);
-            umma_commit(&s_full[t]);
+            if (leader()) umma_commit(&s_full[t]);
           }
-          umma_commit(&empty[s]);
-          if (u.j1 - u.j0 == 1) umma_commit(q_free);
+          if (leader()) umma_commit(&empty[s]);
+          if (u.j1 - u.j0 == 1 && leader()) umma_commit(q_free);
           ++it;
         }
         for (int j = u.j0; j < u.j1; ++j) {
@@ -328,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++it;
               }
               issue_s(t, sk);   // overwrites P_t(j) after PV_t(j) in issue order
-              umma_commit(&s_full[t]);
+              if (leader()) umma_commit(&s_full[t]);
             } else if (pv) {
-              umma_commit(&o_final[t]);
+              if (leader()) umma_commit(&o_final[t]);
             }
           }
           if (j + 1 < u.j1 && sk < 0) {   // K_{j+1} is in the ring for the other tile only: release it
@@ -338,9 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&full[sk], (it / NS) & 1, abort_flag, p.status, status_code(0x16));
             ++it;
           }
-          umma_commit(&empty[sv]);
-          if (sk >= 0) umma_commit(&empty[sk]);
-          if (j + 2 == u.j1) umma_commit(q_free);   // the unit's last S MMAs were just issued
+          if (leader()) umma_commit(&empty[sv]);
+          if (sk >= 0 && leader()) umma_commit(&empty[sk]);
+          if (j + 2 == u.j1 && leader()) umma_commit(q_free);   // the unit's last S MMAs were just issued
         }
       }
     } else if (MK == kMaskStaged && warp == 10 && lane == 0) {

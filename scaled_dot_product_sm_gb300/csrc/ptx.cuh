@@ -169,6 +169,19 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// True in exactly one lane of the (converged) warp: the lowest active lane, so the
+// same lane on every call while the whole warp is active.  A warp that runs an MMA
+// issue loop together and lets this lane issue each tcgen05.mma and commit keeps its
+// operand arithmetic warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
