@@ -16,11 +16,12 @@
 //     in shared memory; the CTA walks the Hq/Hkv query heads of its group and
 //     their 64-row query tiles (last to first, down to the diagonal when
 //     causal), so dK and dV are summed over the group inside the CTA:
-//        S^T  = K Q^T                       (TMEM, 128 keys x 64 queries)
+//        S^T  = K Q^T                       (TMEM, 128 keys x 64 queries, two buffers)
 //        dP^T = V dO^T                      (TMEM)
 //        P^T  = exp2(S^T alpha log2e + mask log2e - lse log2e),  dS^T = P^T o (dP^T - D)
-//        dV  += P^T dO,  dK += dS^T Q       (A operands P^T, dS^T read from TMEM)
-//        dQ^T = K^T dS^T                    (TMEM, 128 head dims x 64 queries; dS^T also in smem)
+//        dV  += P^T dO                      (A operand P^T in TMEM, over the scores it came from)
+//        dK  += dS^T Q,  dQ^T = K^T dS^T    (dS^T in shared memory, two buffers; dQ^T in TMEM,
+//                                            128 head dims x 64 queries)
 //     dQ^T goes from TMEM to the drain warps' registers and is added (without
 //     alpha) to the global fp32 accumulator by reductions in L2: for each query
 //     a warp adds 32 consecutive floats, one full 128-byte line.  Nothing is
@@ -39,17 +40,21 @@
 //   warp  13    TMEM allocator and issuer of the gradient MMAs (dV, dK, dQ^T)
 //   warp  14    issuer of the score MMAs (S^T, dP^T)
 //   warp  15    idle (it completes the fourth warpgroup)
-// TMEM (512 columns): dK [0,128), dV [128,256), S^T [256,320), dP^T [320,384),
-// dQ^T [384,448), P^T bf16 [448,480), dS^T bf16 [480,512).
-// Two threads issue MMAs into the one tensor pipe: the score issuer puts
-// S^T(i+1) and dP^T(i+1) in as soon as the elementwise warps have read S^T(i)
-// and dP^T(i), the gradient issuer puts dV, dK (i) in once P^T(i) and dS^T(i)
-// are stored.  The pipe accepts only a few MMAs ahead, so with one issuer every
-// barrier it waited on let the pipe run dry; with two, one thread's wait does
-// not stop the other's work.  The two streams touch disjoint TMEM columns and
-// everything that orders them goes through the elementwise warps' barriers
-// (the gradient MMAs of tile i start after P^T(i), which needs S^T(i) and
-// dP^T(i) complete), so each thread's commits only have to cover its own MMAs.
+// TMEM (512 columns): dK [0,128), dV [128,256), S^T buffers [256,320) and
+// [320,384) (iteration i uses buffer i & 1), dP^T [384,448), dQ^T [448,512).
+// Two threads issue MMAs into the one tensor pipe.  The score issuer puts S^T(i)
+// in as soon as dV(i-2) has read P^T(i-2) out of the same buffer, which is about
+// an iteration before the elementwise warps need it, and dP^T(i) once they have
+// read dP^T(i-1); the gradient issuer puts dV(i) in once P^T(i) is stored, then
+// dK(i) and dQ^T(i) once dS^T(i) is in shared memory.  The pipe accepts only a
+// few MMAs ahead, so with one issuer every barrier it waited on let the pipe
+// run dry; with two, one thread's wait does not stop the other's work.  Each
+// double buffer has a barrier pair per buffer, so no wait ever has to tell apart
+// two phases of one barrier.  dK reads dS^T from shared memory (where dQ^T needs
+// it anyway) rather than from a TMEM copy: the 32 columns go to the second S^T
+// buffer.  Against one S^T buffer, P^T and dS^T in TMEM and the row statistics
+// inside each 1 KB-padded query-tile stage, this layout took the causal E = 128
+// backward from 0.636 to 0.610 ms and the non-causal one from 1.240 to 1.172 ms.
 #include <cuda.h>
 
 #include <algorithm>
@@ -86,20 +91,29 @@ struct BwdCfg {
   static constexpr int NSQ = 3;
   static constexpr int kKBytes = ECH * BKV * 128;             // K tile: ECH blocks of [128 keys x 64 dims]
   static constexpr int kQTile = ECH * BQ * 128;               // Q (or dO) tile: ECH blocks of [64 rows x 64 dims]
-  static constexpr int kStage = 2 * kQTile + 1024;            // Q, dO, rowstats (512 B, padded)
+  static constexpr int kStage = 2 * kQTile;                   // Q, dO
   static constexpr int kMaskBytes = MSTAGE ? BQ * BKV * 4 : 0;   // additive mask [64 queries x 128 keys] fp32
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKBytes;
   static constexpr int kOffStage = kOffV + kKBytes;
-  static constexpr int kOffDS = kOffStage + NSQ * kStage;     // dS^T [128 keys x 64 queries] bf16
-  static constexpr int kOffMask = kOffDS + BKV * 128;         // mask tile (TMA, one iteration ahead)
+  // dS^T [128 keys x 64 queries] bf16, 128-byte swizzled, two buffers
+  static constexpr int NDS = 2;
+  static constexpr int kOffDS = kOffStage + NSQ * kStage;
+  static constexpr int kOffRS = kOffDS + NDS * BKV * 128;     // row statistics of each stage (512 B)
+  static constexpr int kOffMask = kOffRS + NSQ * BQ * 8;      // mask tile (TMA, one iteration ahead)
   static constexpr int kOffBar = kOffMask + kMaskBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static_assert(E == 64 || E == 128, "head width");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 // TMEM columns
-constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 320, kColDQ = 384, kColP = 448, kColDS = 480;
+constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 384, kColDQ = 448;   // S^T: two 64-column buffers
+// P^T(i) (bf16 pairs) overwrites the S^T buffer it came from: warp half hf puts its 32 queries'
+// 16 columns at hf*32, inside the columns it read, so no other warp's scores are overwritten.
+__device__ __forceinline__ uint32_t p_col(int buf, int kk16) {   // column of P^T queries 16*kk16..
+  return kColS + buf * 64 + (kk16 >> 1) * 32 + (kk16 & 1) * 8;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -193,15 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bar;                 // 1
   uint64_t* q_full = bar + 1;              // kNSQ
   uint64_t* q_empty = q_full + kNSQ;       // kNSQ
-  uint64_t* s_full = q_empty + kNSQ;       // 1
-  uint64_t* s_free = s_full + 1;           // 1
-  uint64_t* dp_full = s_free + 1;          // 1
+  uint64_t* s_full = q_empty + kNSQ;       // 2: S^T(i) complete in buffer i & 1
+  uint64_t* dp_full = s_full + 2;          // 1
   uint64_t* dp_free = dp_full + 1;         // 1
-  uint64_t* pt_full = dp_free + 1;         // 1: P^T(i) in TMEM (one arrival per elementwise warp)
-  uint64_t* pt_free = pt_full + 1;         // 1: dV(i) complete (P^T columns free)
-  uint64_t* ds_full = pt_free + 1;         // 1: dS^T(i) in TMEM and shared memory
-  uint64_t* ds_free = ds_full + 1;         // 1: dK(i) and dQ^T(i) complete (dS^T buffers free)
-  uint64_t* dq_full = ds_free + 1;         // 1
+  uint64_t* pt_full = dp_free + 1;         // 2: P^T(i) in buffer i & 1 (one arrival per elementwise warp)
+  uint64_t* pt_free = pt_full + 2;         // 2: dV(i) complete (buffer i & 1 free for S^T(i + 2))
+  uint64_t* ds_full = pt_free + 2;         // 2: dS^T(i) in shared-memory buffer i % NDS
+  uint64_t* ds_free = ds_full + 2;         // 2: dK(i) and dQ^T(i) complete (that buffer free)
+  uint64_t* dq_full = ds_free + 2;         // 1
   uint64_t* dq_free = dq_full + 1;         // 1
   uint64_t* kdv_done = dq_free + 1;        // 1
   uint64_t* m_full = kdv_done + 1;         // 1: staged mask tile landed
@@ -248,14 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 8);     // one arrival per elementwise warp
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&pt_full[t], 8);   // one arrival per elementwise warp
+      mbar_init(&pt_free[t], 1);
+      mbar_init(&ds_full[t], 8);
+      mbar_init(&ds_free[t], 1);
+    }
     mbar_init(dp_full, 1);
     mbar_init(dp_free, 8);
-    mbar_init(pt_full, 8);
-    mbar_init(pt_free, 1);
-    mbar_init(ds_full, 8);
-    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);    // one arrival per drain warp
     mbar_init(kdv_done, 1);
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(st + c * BQ * 128, &tmQ, &q_full[s], c * 64, qt * BQ, bh);
           tma_load_3d(st + kQTile + c * BQ * 128, &tmdO, &q_full[s], c * 64, qt * BQ, bh);
         }
-        bulk_load(st + 2 * kQTile, a.rowstats + (static_cast<size_t>(bh) * a.Lpad + qt * BQ) * 2, BQ * 8,
+        bulk_load(smem + C::kOffRS + s * (BQ * 8), a.rowstats + (static_cast<size_t>(bh) * a.Lpad + qt * BQ) * 2, BQ * 8,
                   &q_full[s]);
         if (MSTAGE) {   // mask rows qt*BQ.., keys k0.. of head (b, h); zero-filled past L and S
           mbar_wait(m_empty, (i & 1) ^ 1, abort_flag, p.status, status_code(0x3e));
@@ -329,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const SmemDesc dV_k = smem_desc(smem_u32(smem + kOffV), 16, 1024);            // V [keys x dims], K-major
       const SmemDesc dK_mn = smem_desc(smem_u32(smem + kOffK), BKV * 128, 1024);    // K^T as MN-major A
       const SmemDesc dDS_mn = smem_desc(smem_u32(smem + kOffDS), BQ * 128, 1024);   // dS^T as MN-major B
+      const SmemDesc dDS_k = smem_desc(smem_u32(smem + kOffDS), 16, 1024);          // dS^T as K-major A
       const SmemDesc dQ_k = smem_desc(stage0, 16, 1024);                           // Q/dO stage 0, K-major
       const SmemDesc dQ_mn = smem_desc(stage0, BQ * 128, 1024);                    // Q/dO stage 0, MN-major
       mbar_wait(kv_full, 0, abort_flag, p.status, status_code(0x32));
@@ -337,16 +352,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&q_full[s], (i / kNSQ) & 1, abort_flag, p.status, status_code(0x33));
         tc_fence_after();
         const SmemDesc q_k = dQ_k + s * kStage, do_k = q_k + kQTile;
-        if (i > 0) {
-          mbar_wait(s_free, (i - 1) & 1, abort_flag, p.status, status_code(0x34));
+        const int sb = i & 1;
+        if (i >= 2) {   // dV(i-2) has read P^T(i-2) from this buffer
+          mbar_wait(&pt_free[sb], ((i >> 1) - 1) & 1, abort_flag, p.status, status_code(0x34));
           tc_fence_after();
         }
 #pragma unroll
         for (int kk = 0; kk < E / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * (BKV * 128) + (kk & 3) * 32, kb = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          umma_ss(tmem + kColS, dK_k + ka, q_k + kb, id_s, kk > 0);
+          umma_ss(tmem + kColS + sb * 64, dK_k + ka, q_k + kb, id_s, kk > 0);
         }
-        umma_commit(s_full);
+        umma_commit(&s_full[sb]);
         if (i > 0) {
           mbar_wait(dp_free, (i - 1) & 1, abort_flag, p.status, status_code(0x35));
           tc_fence_after();
@@ -364,19 +380,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n; ++i) {               // gradient MMAs
           const int s = i % kNSQ;
           const SmemDesc q_mn = dQ_mn + s * kStage, do_mn = q_mn + kQTile;
+          const int sb = i & 1, db = i % C::NDS;
+          const SmemDesc ds_k = dDS_k + db * (BKV * 128), ds_mn = dDS_mn + db * (BKV * 128);
           // dV += P^T dO as soon as P^T is in TMEM (the elementwise warps are still on dS)
-          mbar_wait(pt_full, i & 1, abort_flag, p.status, status_code(0x36));
+          mbar_wait(&pt_full[sb], (i >> 1) & 1, abort_flag, p.status, status_code(0x36));
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)     // K = queries; 16 queries = 8 TMEM columns
-            umma_ts(tmem + kColDV, tmem + kColP + kk * 8, do_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(pt_free);
-          // dK += dS^T Q
-          mbar_wait(ds_full, i & 1, abort_flag, p.status, status_code(0x40));
+            umma_ts(tmem + kColDV, tmem + p_col(sb, kk), do_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&pt_free[sb]);
+          // dK += dS^T Q, dS^T from shared memory (K-major: 128 key rows of 64 queries)
+          mbar_wait(&ds_full[db], (i / C::NDS) & 1, abort_flag, p.status, status_code(0x40));
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)
-            umma_ts(tmem + kColDK, tmem + kColDS + kk * 8, q_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_ss(tmem + kColDK, ds_k + kk * 32, q_mn + kk * 16 * 128, id_kv, (i > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&q_empty[s]);   // Q and dO of the stage are read
           if (i > 0) {
             mbar_wait(dq_free, (i - 1) & 1, abort_flag, p.status, status_code(0x37));
@@ -384,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)    // dQ^T = K^T dS^T   (K = keys)
-            umma_ss(tmem + kColDQ, dK_mn + kk * 16 * 128, dDS_mn + kk * 16 * 128, id_q, kk > 0);
-          umma_commit(ds_free);
+            umma_ss(tmem + kColDQ, dK_mn + kk * 16 * 128, ds_mn + kk * 16 * 128, id_q, kk > 0);
+          umma_commit(&ds_free[db]);
           umma_commit(dq_full);
         }
         umma_commit(kdv_done);
@@ -398,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;
     const int key = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    uint8_t* dsrow = smem + kOffDS + r * 128;
+    uint8_t* dsrow0 = smem + kOffDS + r * 128;
     const float sc = p.scale_log2;
     TileIter ti = tile0;
     for (int i = 0; i < n; ++i, ti.next()) {
@@ -406,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = ti.qt, g = ti.g;
       const int h = hkv * p.G + g;
       const int q0 = qt * BQ;
-      const float* rs = reinterpret_cast<const float*>(smem + kOffStage + s * kStage + 2 * kQTile);
+      const float* rs = reinterpret_cast<const float*>(smem + C::kOffRS + s * (BQ * 8));
       const int qc = q0 + hf * kHalf;          // first query of this warp's columns
       mbar_wait(&q_full[s], (i / kNSQ) & 1, abort_flag, p.status, status_code(0x38));
       // this warp's 32 values -lse*log2e (plus mask*log2e for its key), read before
@@ -455,18 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t == lane) col = bal;
         }
       }
-      mbar_wait(s_full, i & 1, abort_flag, p.status, status_code(0x39));
+      const int sb = i & 1, db = i % C::NDS;
+      mbar_wait(&s_full[sb], (i >> 1) & 1, abort_flag, p.status, status_code(0x39));
       tc_fence_after();
       float x[kHalf];
       {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kColS + hf * kHalf, v);
+        tmem_ld32(tmem + lane_off + kColS + sb * 64 + hf * kHalf, v);
 #pragma unroll
         for (int j = 0; j < kHalf; ++j) x[j] = __uint_as_float(v[j]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
       // t = s alpha log2e + mask log2e - lse log2e
 #pragma unroll
       for (int j = 0; j < kHalf; j += 2) fma2(x[j], x[j + 1], x[j], x[j + 1], sc, sc, nl[j], nl[j + 1]);
@@ -490,15 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pp[kHalf / 2];
 #pragma unroll
         for (int c = 0; c < kHalf / 2; ++c) pp[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
-        if (i > 0) {   // dV(i-1) has read the previous P^T
-          mbar_wait(pt_free, (i - 1) & 1, abort_flag, p.status, status_code(0x3b));
-          tc_fence_after();
-        }
-        tmem_st16(tmem + lane_off + kColP + hf * (kHalf / 2), pp);
+        // over the scores this warp read (its own columns of the buffer)
+        tmem_st16(tmem + lane_off + kColS + sb * 64 + hf * kHalf, pp);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pt_full);
+        if (lane == 0) mbar_arrive(&pt_full[sb]);
       }
       float nd[kHalf];   // -D of this warp's 32 queries
 #pragma unroll
@@ -541,25 +554,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int c = 0; c < kHalf / 2; ++c) pd[c] = pack_bf16x2(d[2 * c], d[2 * c + 1]);
-      if (i > 0) {   // dK(i-1) and dQ^T(i-1) have read the previous dS^T
-        mbar_wait(ds_free, (i - 1) & 1, abort_flag, p.status, status_code(0x41));
+      if (i >= C::NDS) {   // dK and dQ^T of iteration i - NDS have read this dS^T buffer
+        mbar_wait(&ds_free[db], ((i / C::NDS) - 1) & 1, abort_flag, p.status, status_code(0x41));
         tc_fence_after();
       }
-      if constexpr (DROP) tmem_st16(tmem + lane_off + kColP + hf * (kHalf / 2), pp);   // dV(i-1) is done too
-      tmem_st16(tmem + lane_off + kColDS + hf * (kHalf / 2), pd);
+      if constexpr (DROP) {   // (P o m)^T over this warp's scores, as above
+        tmem_st16(tmem + lane_off + kColS + sb * 64 + hf * kHalf, pp);
+        tmem_wait_st();
+      }
+      uint8_t* dsrow = dsrow0 + db * (BKV * 128);
 #pragma unroll
       for (int c = 0; c < kHalf / 8; ++c) {
         const int chunk = hf * (kHalf / 8) + c;
         const uint4 u = make_uint4(pd[4 * c], pd[4 * c + 1], pd[4 * c + 2], pd[4 * c + 3]);
         *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (r & 7)) << 4)) = u;
       }
-      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (DROP) mbar_arrive(pt_full);
-        mbar_arrive(ds_full);
+        if (DROP) mbar_arrive(&pt_full[sb]);
+        mbar_arrive(&ds_full[db]);
       }
     }
     // ---------------------------------------------------------- dK, dV epilogue (one column half writes)
