@@ -270,8 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 9 && (kWarpIssue || lane == 0)) {
     // ------------------------------------------------------------ MMA issuer
-      // the one lane that issues (all of them, when lane 0 alone runs this loop)
-      auto leader = [&]() { return !kWarpIssue || elect_one(); };
+      // The one lane that issues: elected once (lane 0 of the converged warp), so every
+      // MMA and commit comes from the same thread, as a commit only covers its own thread's
+      // MMAs.  Electing once measured faster than an elect.sync per MMA (C3 forward 0.188
+      // -> 0.185 ms), and much faster than testing lane == 0 (0.232 ms).
+      const bool lead = !kWarpIssue || elect_one();
+      auto leader = [&]() { return lead; };
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);        // Q (K-major) x K (K-major)
       constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (TMEM, K-major) x V (MN-major)
       // Operand descriptors, built once; a K-step, a tile or a ring slot moves only the start address.
