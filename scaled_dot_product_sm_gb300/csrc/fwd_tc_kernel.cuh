@@ -35,12 +35,10 @@
 // The issuer paces the whole kernel: each tile's chain is its softmax, then
 // PV_t(j) and S_t(j+1) behind the other tile's MMAs, so every cycle the issuing
 // thread spends between MMA groups (barrier waits, commits, descriptor
-// arithmetic) lengthens it.  Without a staged mask the whole of warp 9 runs
-// the issue loop, converged, and the lane elect.sync picks issues each MMA and
-// commit: the operand arithmetic is then warp-uniform, and the causal E = 128
-// forward runs 7.5 % faster than with lane 0 alone in a divergent branch.  With
-// the staged mask, where the softmax rather than the issuer sets the pace, lane 0
-// alone measured 1 % faster, so that instantiation keeps it.
+// arithmetic) lengthens it.  The whole of warp 9 runs the issue loop, converged,
+// and the lane elect.sync picked once issues each MMA and commit: the operand
+// arithmetic is then warp-uniform, and the causal E = 128 forward runs 8 % faster
+// than with lane 0 alone in a divergent branch (the masked one 2.7 %).
 #pragma once
 
 #include <cuda.h>
@@ -99,7 +97,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM, FwdParams p) {
   constexpr bool MASKED = MK != kMaskNone;
-  constexpr bool kWarpIssue = MK != kMaskStaged;   // the MMA issuer: all of warp 9, or lane 0 alone
   using C = FwdCfg<ECH, VCH, MK>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -268,13 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nunits > 0) mbar_drain(bar_q, static_cast<uint32_t>((nunits - 1) & 1));
         mbar_drain_ring(full, NS, it);
       }
-    } else if (warp == 9 && (kWarpIssue || lane == 0)) {
+    } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
       // The one lane that issues: elected once (lane 0 of the converged warp), so every
       // MMA and commit comes from the same thread, as a commit only covers its own thread's
       // MMAs.  Electing once measured faster than an elect.sync per MMA (C3 forward 0.188
       // -> 0.185 ms), and much faster than testing lane == 0 (0.232 ms).
-      const bool lead = !kWarpIssue || elect_one();
+      const bool lead = elect_one();
       auto leader = [&]() { return lead; };
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);        // Q (K-major) x K (K-major)
       constexpr uint32_t idesc_o = idesc_bf16(BM, C::Ev, 0, 1);     // P (TMEM, K-major) x V (MN-major)
