@@ -558,18 +558,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_use = need ? m_new : m_run;
         const float nm = (m_use == kNegInf) ? 0.f : -m_use;
         const float corr = need ? ex2(m_run + nm) : 1.f;
-        // p = exp2(x - m), packed to bf16 pairs; row sum in eight independent chains
+        // p = exp2(x - m), packed to bf16 pairs; row sum in eight independent chains.  In
+        // three passes (all exponents, all exponentials, then sums and packing), which
+        // measured 1 % faster than one pass per pair (C3 forward 0.1867 -> 0.1846 ms).
         uint32_t pk[BN / 2];
         float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
+        for (int i = 0; i < BN; i += 2) fma2(x[i], x[i + 1], x[i], x[i + 1], xs, xs, nm, nm);   // x * xs - m
+#pragma unroll
+        for (int i = 0; i < BN; ++i) x[i] = ex2(x[i]);
+#pragma unroll
         for (int i = 0; i < BN; i += 2) {
-          float a0, a1;
-          fma2(a0, a1, x[i], x[i + 1], xs, xs, nm, nm);   // x * xs - m
-          a0 = ex2(a0);
-          a1 = ex2(a1);
           const int q4 = (i >> 1) & 3;
-          add2(rs8[2 * q4], rs8[2 * q4 + 1], rs8[2 * q4], rs8[2 * q4 + 1], a0, a1);
-          pk[i >> 1] = pack_bf16x2(a0, a1);
+          add2(rs8[2 * q4], rs8[2 * q4 + 1], rs8[2 * q4], rs8[2 * q4 + 1], x[i], x[i + 1]);
+          pk[i >> 1] = pack_bf16x2(x[i], x[i + 1]);
         }
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l_run = l_run * corr + rs;
