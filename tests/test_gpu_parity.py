@@ -190,6 +190,28 @@ def test_bf16_prefill(case):
     run_case(B, Hq, Hkv, L, S, E, Ev, torch.bfloat16, causal, mk, ms, fr, seed=7)
 
 
+# One, two and three iterations per backward CTA (64-row query tiles times the heads of
+# its group): the two S^T buffers, the two dS^T buffers and, with a staged mask, the
+# dS^T hand-over deferred to the next iteration, each at its first uses and at the end.
+ITER_CASES = [
+    # B, Hq, Hkv, L, S, E, causal, mask kind, mask shape
+    (1, 1, 1, 64, 64, 128, False, "none", None),       # 1 iteration
+    (1, 1, 1, 128, 128, 128, False, "none", None),     # 2
+    (1, 1, 1, 192, 192, 64, False, "none", None),      # 3
+    (2, 3, 1, 64, 64, 128, False, "none", None),       # 3: one query tile, three heads
+    (1, 2, 1, 320, 320, 128, True, "none", None),      # 10 down to 2 per key tile
+    (1, 1, 1, 64, 64, 128, False, "bias", (1, 1)),     # staged mask, 1 iteration
+    (1, 1, 1, 128, 128, 128, False, "bias", (1, 1)),   # 2
+    (2, 2, 2, 192, 192, 64, False, "block", (2, 2)),   # 3
+]
+
+
+@pytest.mark.parametrize("case", ITER_CASES, ids=[str(i) for i in range(len(ITER_CASES))])
+def test_backward_iteration_counts(case):
+    B, Hq, Hkv, L, S, E, causal, mk, ms = case
+    run_case(B, Hq, Hkv, L, S, E, E, torch.bfloat16, causal, mk, ms, 0, seed=21)
+
+
 def test_bf16_large_scores_no_overflow():
     """Scores of order 1e3-1e4 stay finite and match (the max is subtracted first)."""
     q, k, v, dO, _ = random_inputs(1, 2, 2, 200, 300, 64, 64, torch.bfloat16, seed=9)
