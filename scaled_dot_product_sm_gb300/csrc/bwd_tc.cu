@@ -193,7 +193,8 @@ template <int E_, bool DROP, bool MSTAGE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-                  const __grid_constant__ CUtensorMap tmM, TcBwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmdK,
+                  const __grid_constant__ CUtensorMap tmdV, TcBwdArgs a) {
   using C = BwdCfg<E_, MSTAGE>;
   constexpr int kNSQ = C::NSQ;
   constexpr int E = C::E, Ev = C::Ev, ECH = C::ECH;
@@ -590,19 +591,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!kDeferDS) hand_over();
     }
     if (pend >= 0) hand_over();
-    // ---------------------------------------------------------- dK, dV epilogue (one column half writes)
-    if (hf == 0) {
-    __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bkv) * p.S + key) * E;
-    __nv_bfloat16* dvrow = static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bkv) * p.S + key) * Ev;
+    // ---------------------------------------------------------- dK, dV epilogue
+    // Warps hf = 0 take dK and warps hf = 1 dV, each its 32 keys: scaled, packed to bf16
+    // and written as 128-byte-swizzled [128 keys x 64 dims] blocks into the query-tile
+    // stages (idle once the last MMA is complete), which one thread then stores with TMA
+    // (rows past S are not written).  Stored row by row from registers, each warp
+    // instruction wrote 16 bytes into 32 different lines and the epilogue took about 4 us.
     if (n > 0) {
       mbar_wait(kdv_done, 0, abort_flag, p.status, status_code(0x3c));
       tc_fence_after();
     }
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const uint32_t col = m == 0 ? kColDK : kColDV;
-      const float sc2 = m == 0 ? p.scale : 1.f;
-      __nv_bfloat16* dst = m == 0 ? dkrow : dvrow;
+    {
+      const uint32_t col = hf == 0 ? kColDK : kColDV;
+      const float sc2 = hf == 0 ? p.scale : 1.f;
+      uint8_t* blk = smem + kOffStage + hf * kKBytes;   // ECH blocks of [128 keys x 64 dims]
 #pragma unroll
       for (int c = 0; c < E / 32; ++c) {
         uint32_t v[32];
@@ -612,19 +614,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0u;
         }
-        if (key < p.S) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[u * 8 + 0]) * sc2, __uint_as_float(v[u * 8 + 1]) * sc2);
-            w.y = pack_bf16x2(__uint_as_float(v[u * 8 + 2]) * sc2, __uint_as_float(v[u * 8 + 3]) * sc2);
-            w.z = pack_bf16x2(__uint_as_float(v[u * 8 + 4]) * sc2, __uint_as_float(v[u * 8 + 5]) * sc2);
-            w.w = pack_bf16x2(__uint_as_float(v[u * 8 + 6]) * sc2, __uint_as_float(v[u * 8 + 7]) * sc2);
-            *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = w;
-          }
+        for (int u = 0; u < 4; ++u) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[u * 8 + 0]) * sc2, __uint_as_float(v[u * 8 + 1]) * sc2);
+          w.y = pack_bf16x2(__uint_as_float(v[u * 8 + 2]) * sc2, __uint_as_float(v[u * 8 + 3]) * sc2);
+          w.z = pack_bf16x2(__uint_as_float(v[u * 8 + 4]) * sc2, __uint_as_float(v[u * 8 + 5]) * sc2);
+          w.w = pack_bf16x2(__uint_as_float(v[u * 8 + 6]) * sc2, __uint_as_float(v[u * 8 + 7]) * sc2);
+          const int chunk = (c & 1) * 4 + u;   // 16-byte chunk of this key's 128-byte row in block c / 2
+          *reinterpret_cast<uint4*>(blk + (c >> 1) * (BKV * 128) + r * 128 + ((chunk ^ (r & 7)) << 4)) = w;
         }
       }
-    }
+      fence_proxy_async_smem();   // generic writes, then the TMA (async proxy) reads them
+      named_bar_sync(2, 256);     // the eight elementwise warps
+      if (warp == 0 && lane == 0) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int cb = 0; cb < ECH; ++cb)
+            tma_store_3d(t == 0 ? &tmdK : &tmdV, smem + kOffStage + t * kKBytes + cb * (BKV * 128), cb * 64, k0,
+                         bkv);
+        bulk_commit_and_wait_read();   // the stages stay in use until the TMA has read them
+      }
     }
   } else if (warp < 12) {
     regs_inc<kRegsDrain>();
@@ -684,8 +695,10 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
   bwd_rowstats_kernel<E><<<static_cast<unsigned>((srows + 7) / 8), 256, 0, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  alignas(64) CUtensorMap tmK, tmV, tmQ, tmdO;
-  if (!encode_tmap_bf16_3d(&tmK, p.k, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
+  alignas(64) CUtensorMap tmK, tmV, tmQ, tmdO, tmdK, tmdV;
+  if (!encode_tmap_bf16_3d(&tmdK, p.dk, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
+      !encode_tmap_bf16_3d(&tmdV, p.dv, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
+      !encode_tmap_bf16_3d(&tmK, p.k, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
       !encode_tmap_bf16_3d(&tmV, p.v, E, p.S, static_cast<uint64_t>(p.B) * p.Hkv, 64, BKV) ||
       !encode_tmap_bf16_3d(&tmQ, p.q, E, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BQ) ||
       !encode_tmap_bf16_3d(&tmdO, p.dO, E, p.L, static_cast<uint64_t>(p.B) * p.Hq, 64, BQ))
@@ -711,7 +724,7 @@ cudaError_t run_bwd(const BwdParams& p, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if ((e = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, tmQ, tmdO, tmM, a)) != cudaSuccess) return e;
+  if ((e = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, tmQ, tmdO, tmM, tmdK, tmdV, a)) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(p.B) * p.Hq * p.L * E / 8;
   const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n8 + 255) / 256, 152 * 16));
   cudaLaunchConfig_t cfg2 = {};
