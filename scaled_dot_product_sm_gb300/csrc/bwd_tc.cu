@@ -27,7 +27,9 @@
 //     a warp adds 32 consecutive floats, one full 128-byte line.  Nothing is
 //     staged in shared memory, whose bandwidth the SS MMAs (K and Q, V and dO,
 //     K^T and dS^T) already use heavily; the 32 KB saved give the masked
-//     variant its third query-tile stage;
+//     variant its third query-tile stage.  At the end the eight elementwise
+//     warps write dK (times alpha) and dV as bf16 through the idle query-tile
+//     stages, and one thread stores them with TMA;
 //  3. dQ = bf16(alpha * accumulator).
 // The main kernel and the conversion are programmatic dependent launches: each
 // starts while the grid before it finishes, and waits for it (griddepcontrol)
