@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kdv_done = dq_free + 1;        // 1
   uint64_t* m_full = kdv_done + 1;         // 1: staged mask tile landed
   uint64_t* m_empty = m_full + 1;          // 1: mask tile read by the elementwise warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(m_empty + 1);
+  uint64_t* mma_drain = m_empty + 1;       // 2: every MMA of the score / gradient issuer complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -280,6 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(kdv_done, 1);
     mbar_init(m_full, 1);
     mbar_init(m_empty, 8);
+    mbar_init(&mma_drain[0], 1);
+    mbar_init(&mma_drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -381,6 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (warp == 14) {
         for (int i = 0; i < n; ++i) issue_sdp(i);   // score MMAs
+        // every MMA this thread issued is complete before the CTA releases TMEM (after a
+        // wait that gave up, some may still be queued; the drain is bounded like every wait)
+        umma_commit(&mma_drain[0]);
+        mbar_drain(&mma_drain[0], 0);
       } else {
         for (int i = 0; i < n; ++i) {               // gradient MMAs
           const int s = i % kNSQ;
@@ -412,6 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(dq_full);
         }
         umma_commit(kdv_done);
+        umma_commit(&mma_drain[1]);   // as for the score issuer
+        mbar_drain(&mma_drain[1], 0);
       }
     }
   } else if (warp < 8) {

@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mk_empty = mk_full + 4;      // 4: ... and read by tile t's softmax warps
   uint64_t* un_full = mk_empty + 4;      // 4: unit index published (taken from the counter)
   uint64_t* un_empty = un_full + 4;      // 4: ... and read by every role
-  int* un_slot = reinterpret_cast<int*>(un_empty + 4);                  // 4 unit indices
+  uint64_t* mma_drain = un_empty + 4;    // 1: every MMA of the issuing thread complete (before TMEM is released)
+  int* un_slot = reinterpret_cast<int*>(mma_drain + 1);                 // 4 unit indices
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(un_slot + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&un_empty[i], 9 + (MK == kMaskStaged ? 1 : 0));   // MMA thread, 8 softmax warps, mask producer
       un_slot[i] = -1;
     }
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -356,6 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 2 == u.j1 && leader()) umma_commit(q_free);   // the unit's last S MMAs were just issued
         }
       }
+      // every MMA this thread issued is complete before the CTA releases TMEM (after a wait
+      // that gave up, some may still be queued; the drain is bounded like every wait)
+      if (leader()) umma_commit(mma_drain);
+      mbar_drain(mma_drain, 0);
     } else if (MK == kMaskStaged && warp == 10 && lane == 0) {
     // ------------------------------------------------------------ mask producer
       // One buffer in two halves (keys 0-63 and 64-127 of a key tile), filled in the
