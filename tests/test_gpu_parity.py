@@ -181,6 +181,12 @@ BF16_CASES = [
     # more work units than SMs: the persistent forward walks several units per CTA
     (2, 96, 32, 300, 333, 128, 128, True, "bias", (2, 1), 2),
     (1, 200, 200, 130, 140, 64, 64, False, "none", None, 0),
+    # large query groups: sixteen query heads on one KV head (MQA), eight per KV head with a
+    # per-head mask (S not a multiple of 4: the mask is read from global memory)
+    (1, 16, 1, 200, 300, 128, 128, True, "none", None, 0),
+    (2, 8, 1, 150, 150, 64, 64, False, "bias", (2, 8), 1),
+    # one query row under the causal mask: key 0 alone is open, dK = dV = 0 past it
+    (2, 4, 2, 1, 100, 128, 128, True, "none", None, 0),
 ]
 
 
@@ -245,6 +251,17 @@ def test_decode_with_mask_and_rows():
     ref_o, ref_lse = oracle.ref_forward(q, k, v, mask, None, False, True)
     o, lse = sdpa.sdpa_decode(q.cuda(), k.cuda(), v.cuda(), mask.cuda(), None, True, 3)
     check_forward(o, lse, ref_o, ref_lse, True)
+
+
+def test_decode_mqa_groups():
+    """Decode with 32 query heads on one KV head (four row groups of 8 per split) and a ragged
+    S, for the automatic split count and for an explicit one."""
+    B, Hq, Hkv, S, E = 2, 32, 1, 2049, 128
+    q, k, v, _, _ = random_inputs(B, Hq, Hkv, 1, S, E, E, torch.bfloat16, seed=14)
+    ref_o, ref_lse = oracle.ref_forward(q, k, v, None, None, False, True)
+    for splits in (0, 5):
+        o, lse = sdpa.sdpa_decode(q.cuda(), k.cuda(), v.cuda(), None, None, True, splits)
+        check_forward(o, lse, ref_o, ref_lse, True)
 
 
 def test_forward_routes_l1_to_decode():
